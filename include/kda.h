@@ -1,0 +1,184 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention operator library.
+ *
+ * The operator ("Kimi K3: KDA, attention residuals and Stable LatentMoE",
+ * hs-black.github.io, Sec. 2.1-2.3), per sequence and head, dk = dv = d:
+ *
+ *   alpha_t = exp(g_t),  g_t = g_min * Sigmoid(exp(A_h) * z_t)        (Sec. 2.2)
+ *   S_t     = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   o_t     = scale * S_t^T q_t                                        (Sec. 2.1)
+ *   y_t     = Sigmoid(g_in_t) (.) w (.) o_t / sqrt(mean(o_t^2) + eps)  (Sec. 2.3)
+ *
+ * with q, k optionally L2-normalised per token: x / sqrt(sum x^2 + 1e-6).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *    comment says otherwise.  The library never allocates device memory and
+ *    keeps no state between calls.
+ *  - All work is enqueued on the caller's `stream` (cudaStream_t passed as
+ *    void*; NULL = legacy default stream).  Calls return as soon as the work
+ *    is enqueued; arguments are validated on the host before anything is
+ *    enqueued, and nothing is enqueued when validation fails.
+ *  - Tensors are dense, row-major, last index fastest, with the layouts below;
+ *    every pointer must be 16-byte aligned.
+ *  - No call throws.  Errors are reported through kda_status; a failed launch
+ *    returns KDA_ERR_CUDA (the CUDA error string is available from
+ *    kda_last_error_string()).
+ *  - Calls on distinct streams may run concurrently; the library is
+ *    thread-safe.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,        /* a required pointer is NULL                        */
+    KDA_ERR_SHAPE = 2,       /* unsupported or inconsistent sizes                 */
+    KDA_ERR_DTYPE = 3,       /* unsupported dtype combination                     */
+    KDA_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned                  */
+    KDA_ERR_SEQLENS = 5,     /* cu_seqlens not monotone / not ending at tokens    */
+    KDA_ERR_UNSUPPORTED = 6, /* valid request the library does not implement      */
+    KDA_ERR_CUDA = 7,        /* a CUDA runtime call or a launch failed            */
+    KDA_ERR_WORKSPACE = 8    /* workspace missing or smaller than required        */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+/*
+ * Chunked prefill over packed sequences (Sec. 2.1 chunked form, Sec. 2.2
+ * 16-token sub-chunks; chunk length 64).
+ *
+ * Token layout: the T_total tokens of num_seqs sequences are packed; sequence n
+ * owns tokens [cu_seqlens[n], cu_seqlens[n+1]).  cu_seqlens is a DEVICE int32
+ * array of num_seqs+1 entries and a HOST copy (cu_seqlens_host) of the same
+ * values is required too: the host copy sizes the launch and is validated
+ * (cu_seqlens_host[0] == 0, non-decreasing, last == T_total); the device copy
+ * must hold identical values.
+ *
+ *   q, k  [T_total, H, dk]   dtype qkv_dtype
+ *   v     [T_total, H, dv]   dtype qkv_dtype
+ *   z     [T_total, H, dk]   float32  decay logits (bias included)
+ *   beta  [T_total, H]       float32  write strengths in (0, 1)
+ *   A     [H]                float32  per-head log scale
+ *   S0    [num_seqs, H, dk, dv] float32 initial states, or NULL (zero state)
+ *   o     [T_total, H, dv]   dtype qkv_dtype (output)
+ *   S_T   [num_seqs, H, dk, dv] float32 final states (output), or NULL;
+ *         S_T may equal S0 (in-place state update).
+ *   g_in  [T_total, H, dv]   bf16 gate pre-activations, or NULL (no fused gate)
+ *   norm_w [dv] float32 RMSNorm weight, or NULL (ones); used with g_in
+ *   y     [T_total, H, dv]   bf16 fused output gate result (required iff g_in)
+ *
+ * Supported: dk = dv = 128 with bf16 q/k/v (tensor-core chunked path), and
+ * dk = dv in {32, 64, 128} with float32 q/k/v (CUDA-core path); H >= 1.
+ * workspace: device scratch of kda_prefill_workspace_size() bytes (may be
+ * NULL when that size is 0).
+ */
+typedef struct {
+    int num_seqs;
+    int T_total;
+    int H, dk, dv;
+    kda_dtype qkv_dtype;
+    const int32_t* cu_seqlens;       /* device */
+    const int32_t* cu_seqlens_host;  /* host   */
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* z;
+    const float* beta;
+    const float* A;
+    float g_min;          /* -5 in every workload */
+    float scale;          /* readout scale, 1.0 in every workload */
+    int qk_l2norm;        /* 1: L2-normalise q and k in FP32 (eps 1e-6) */
+    const float* S0;
+    void* o;
+    float* S_T;
+    const void* g_in;
+    const float* norm_w;
+    float norm_eps;       /* RMSNorm epsilon, 1e-6 in every workload */
+    void* y;
+    void* workspace;
+    size_t workspace_bytes;
+} kda_prefill_args;
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* args);
+kda_status kda_prefill(const kda_prefill_args* args, void* stream);
+
+/*
+ * The same operator as kda_prefill, always evaluated by the per-token
+ * recurrence on CUDA cores (one CTA per sequence and head, the state held in
+ * registers).  Same arguments, layouts, validation and status codes as
+ * kda_prefill; the workspace is not used.  Exported to cross-check the
+ * chunked tensor-core path on the GPU; it is sequential in the tokens of each
+ * sequence and therefore slow for long sequences.
+ */
+kda_status kda_prefill_recurrent(const kda_prefill_args* args, void* stream);
+
+/*
+ * Batched single-token decode step (Sec. 2.1 recurrence, one token per
+ * sequence), states updated IN PLACE.
+ *
+ *   q, k, z [N, H, dk] (q, k bf16; z float32); v [N, H, dv] bf16;
+ *   beta [N, H] float32; A [H] float32;
+ *   state [num_slots, H, dk, dv] float32, read and overwritten;
+ *   slots [N] int32 row of `state` used by sequence n, or NULL (row n,
+ *         then num_slots >= N is required); slots must be distinct.  The
+ *         kernel range-checks every slot on the device and skips a sequence
+ *         whose slot lies outside [0, num_slots): its state row, o and y are
+ *         left untouched (no fault, no error code, since the slots live in
+ *         device memory and are not read on the host).
+ *   o [N, H, dv] bf16 output or NULL; g_in/norm_w/y as in prefill
+ *   (y required iff g_in).  At least one of o, y must be given.
+ * Supported: dk = dv = 128.
+ */
+typedef struct {
+    int N, H, dk, dv, num_slots;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* z;
+    const float* beta;
+    const float* A;
+    float g_min;
+    float scale;
+    int qk_l2norm;
+    float* state;
+    const int32_t* slots;
+    void* o;
+    const void* g_in;
+    const float* norm_w;
+    float norm_eps;
+    void* y;
+} kda_decode_args;
+
+kda_status kda_decode_step(const kda_decode_args* args, void* stream);
+
+/*
+ * Output gate alone (Sec. 2.3): y = Sigmoid(g_in) (.) w (.) o / sqrt(mean(o^2)+eps),
+ * the mean taken over the dv channels of each (token, head) row.
+ *   o, g_in, y [rows, dv] (rows = tokens * H) with dtype `dtype` (bf16 or
+ *   float32; all three the same); w [dv] float32 or NULL (ones).
+ * Supported: dv in {32, 64, 128, 256}.
+ */
+kda_status kda_gate_norm(const void* o, const void* g_in, const float* norm_w, float eps,
+                         void* y, long rows, int dv, kda_dtype dtype, void* stream);
+
+/* Static description of a status code. */
+const char* kda_status_str(kda_status s);
+
+/* Text of the last CUDA error seen by this thread inside the library. */
+const char* kda_last_error_string(void);
+
+/* Library build description (architecture, version). */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_H_ */

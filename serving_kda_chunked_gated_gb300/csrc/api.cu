@@ -1,0 +1,145 @@
+// Host side of the C ABI declared in include/kda.h: argument validation and
+// kernel dispatch.  No device memory is allocated here; every launch goes on
+// the caller's stream.
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_decode_step(const kda_decode_args& a, cudaStream_t stream);
+cudaError_t launch_gate_norm(const void* o, const void* g, const float* w, float eps, void* y,
+                             long rows, int dv, bool bf16, cudaStream_t s);
+cudaError_t launch_prefill_recurrent(const kda_prefill_args& a, cudaStream_t s);
+bool prefill_tc_supported(const kda_prefill_args& a);
+size_t prefill_tc_workspace_size(const kda_prefill_args& a);
+cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
+}  // namespace kda
+
+static thread_local char g_last_error[256] = "no error";
+
+static kda_status cuda_fail(cudaError_t e) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return KDA_ERR_CUDA;
+}
+
+static bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+extern "C" {
+
+const char* kda_status_str(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_NULL: return "required pointer is NULL";
+        case KDA_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case KDA_ERR_DTYPE: return "unsupported dtype";
+        case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case KDA_ERR_SEQLENS: return "invalid cu_seqlens";
+        case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KDA_ERR_CUDA: return "CUDA error";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char* kda_last_error_string(void) { return g_last_error; }
+
+const char* kda_version(void) { return "kda-gb300 0.1 (sm_103a; tcgen05 tf32 chunked prefill)"; }
+
+// ---------------------------------------------------------------------------
+// prefill
+// ---------------------------------------------------------------------------
+
+static kda_status validate_prefill(const kda_prefill_args* a) {
+    if (!a) return KDA_ERR_NULL;
+    if (a->num_seqs < 0 || a->T_total < 0 || a->H <= 0) return KDA_ERR_SHAPE;
+    if (a->dk != a->dv) return KDA_ERR_SHAPE;
+    if (a->qkv_dtype != KDA_BF16 && a->qkv_dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!(a->dk == 32 || a->dk == 64 || a->dk == 128)) return KDA_ERR_SHAPE;
+    if (!a->cu_seqlens || !a->cu_seqlens_host) return KDA_ERR_NULL;
+    if (a->T_total > 0 && (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o)) return KDA_ERR_NULL;
+    if (!a->A) return KDA_ERR_NULL;
+    if (a->g_in && !a->y) return KDA_ERR_NULL;
+    if (a->g_in && a->qkv_dtype != KDA_BF16) return KDA_ERR_DTYPE;
+    const void* ptrs[] = {a->q, a->k, a->v, a->z, a->beta, a->A, a->S0, a->o, a->S_T,
+                          a->g_in, a->norm_w, a->y, a->cu_seqlens};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return KDA_ERR_ALIGN;
+    const int32_t* cu = a->cu_seqlens_host;
+    if (cu[0] != 0) return KDA_ERR_SEQLENS;
+    for (int n = 0; n < a->num_seqs; ++n)
+        if (cu[n + 1] < cu[n]) return KDA_ERR_SEQLENS;
+    if (cu[a->num_seqs] != a->T_total) return KDA_ERR_SEQLENS;
+    // S0 may alias S_T exactly; any other overlap between outputs and inputs is rejected.
+    return KDA_OK;
+}
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
+    if (validate_prefill(a) != KDA_OK) return 0;
+    if (kda::prefill_tc_supported(*a)) return kda::prefill_tc_workspace_size(*a);
+    return 0;
+}
+
+kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
+    kda_status st = validate_prefill(a);
+    if (st != KDA_OK) return st;
+    if (a->num_seqs == 0) return KDA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (kda::prefill_tc_supported(*a)) {
+        if (a->workspace_bytes < kda::prefill_tc_workspace_size(*a)) return KDA_ERR_WORKSPACE;
+        if (a->workspace_bytes > 0 && !a->workspace) return KDA_ERR_WORKSPACE;
+        e = kda::launch_prefill_tc(*a, s);
+    } else {
+        e = kda::launch_prefill_recurrent(*a, s);
+    }
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+kda_status kda_prefill_recurrent(const kda_prefill_args* a, void* stream) {
+    kda_status st = validate_prefill(a);
+    if (st != KDA_OK) return st;
+    if (a->num_seqs == 0) return KDA_OK;
+    cudaError_t e = kda::launch_prefill_recurrent(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+
+kda_status kda_decode_step(const kda_decode_args* a, void* stream) {
+    if (!a) return KDA_ERR_NULL;
+    if (a->N < 0 || a->H <= 0 || a->num_slots < 0) return KDA_ERR_SHAPE;
+    if (a->dk != 128 || a->dv != 128) return KDA_ERR_SHAPE;
+    if (!a->slots && a->num_slots < a->N) return KDA_ERR_SHAPE;
+    if (a->N > 0 && (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->A || !a->state))
+        return KDA_ERR_NULL;
+    if (!a->o && !a->y) return KDA_ERR_NULL;
+    if (a->g_in && !a->y) return KDA_ERR_NULL;
+    if (a->y && !a->g_in) return KDA_ERR_NULL;
+    const void* ptrs[] = {a->q, a->k, a->v, a->z, a->beta, a->A, a->state, a->slots, a->o,
+                          a->g_in, a->norm_w, a->y};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return KDA_ERR_ALIGN;
+    cudaError_t e = kda::launch_decode_step(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// gate-norm
+// ---------------------------------------------------------------------------
+
+kda_status kda_gate_norm(const void* o, const void* g_in, const float* norm_w, float eps, void* y,
+                         long rows, int dv, kda_dtype dtype, void* stream) {
+    if (rows < 0) return KDA_ERR_SHAPE;
+    if (!(dv == 32 || dv == 64 || dv == 128 || dv == 256)) return KDA_ERR_SHAPE;
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (rows > 0 && (!o || !g_in || !y)) return KDA_ERR_NULL;
+    if (misaligned(o) || misaligned(g_in) || misaligned(y) || misaligned(norm_w)) return KDA_ERR_ALIGN;
+    cudaError_t e = kda::launch_gate_norm(o, g_in, norm_w, eps, y, rows, dv, dtype == KDA_BF16,
+                                          reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

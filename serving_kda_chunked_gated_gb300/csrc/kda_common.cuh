@@ -1,0 +1,57 @@
+// Device helpers shared by the KDA kernels (decay gate, bf16 I/O, reductions).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+#define KDA_DEV __device__ __forceinline__
+
+namespace kda {
+
+// Logistic function through the hardware exp2 / fast-divide path.
+KDA_DEV float sigmoidf_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// Bounded decay gate ("Kimi K3" page, Sec. 2.2): log-retention
+//   g = g_min * Sigmoid(exp(A_h) * z), g in (g_min, 0).
+// eA is exp(A_h), computed once per head.
+KDA_DEV float log_decay(float z, float eA, float g_min) { return g_min * sigmoidf_fast(eA * z); }
+
+KDA_DEV float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// round-to-nearest-even float -> bf16 bits (finite inputs)
+KDA_DEV uint16_t f_to_bf16(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+KDA_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Load 8 consecutive bf16 (16 bytes) as floats.
+KDA_DEV void load8_bf16(const uint16_t* p, float* out) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+KDA_DEV void store8_bf16(uint16_t* p, const float* in) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = (uint32_t)f_to_bf16(in[2 * i]) | ((uint32_t)f_to_bf16(in[2 * i + 1]) << 16);
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Streaming (read-once / write-once) 128-bit accesses for large state tensors.
+KDA_DEV float4 ld_stream_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+KDA_DEV void st_stream_f4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+
+}  // namespace kda

@@ -1,0 +1,233 @@
+"""Thin Python binding of the KDA C ABI (``include/kda.h``).
+
+Argument marshalling only: every step of the operator runs in the CUDA kernels
+of ``_build/libkda.so``.  Tensors are torch CUDA tensors (PyTorch supplies the
+device memory and the stream); their data pointers are handed to the C entry
+points.  If the library has not been built this module raises on first use --
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_BF16, KDA_F32 = 0, 1
+STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE",
+          4: "KDA_ERR_ALIGN", 5: "KDA_ERR_SEQLENS", 6: "KDA_ERR_UNSUPPORTED",
+          7: "KDA_ERR_CUDA", 8: "KDA_ERR_WORKSPACE"}
+
+EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
+            "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
+            "kda_version"]
+
+_vp = ctypes.c_void_p
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int), ("T_total", ctypes.c_int),
+        ("H", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("qkv_dtype", ctypes.c_int),
+        ("cu_seqlens", _vp), ("cu_seqlens_host", _vp),
+        ("q", _vp), ("k", _vp), ("v", _vp), ("z", _vp), ("beta", _vp), ("A", _vp),
+        ("g_min", ctypes.c_float), ("scale", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
+        ("S0", _vp), ("o", _vp), ("S_T", _vp),
+        ("g_in", _vp), ("norm_w", _vp), ("norm_eps", ctypes.c_float), ("y", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int), ("H", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("num_slots", ctypes.c_int),
+        ("q", _vp), ("k", _vp), ("v", _vp), ("z", _vp), ("beta", _vp), ("A", _vp),
+        ("g_min", ctypes.c_float), ("scale", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
+        ("state", _vp), ("slots", _vp), ("o", _vp),
+        ("g_in", _vp), ("norm_w", _vp), ("norm_eps", ctypes.c_float), ("y", _vp),
+    ]
+
+
+class KDAError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the compiled library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"KDA CUDA library not built: {path} is missing "
+                          "(run serving_kda_chunked_gated_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill_recurrent.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+    lib.kda_prefill_recurrent.restype = ctypes.c_int
+    lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_gate_norm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, ctypes.c_long,
+                                  ctypes.c_int, ctypes.c_int, _vp]
+    lib.kda_gate_norm.restype = ctypes.c_int
+    lib.kda_status_str.argtypes = [ctypes.c_int]
+    lib.kda_status_str.restype = ctypes.c_char_p
+    lib.kda_last_error_string.restype = ctypes.c_char_p
+    lib.kda_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        lib = load_library()
+        msg = lib.kda_status_str(status).decode()
+        if status == 7:
+            msg += ": " + lib.kda_last_error_string().decode()
+        raise KDAError(f"{what} failed with {STATUS.get(status, status)} ({msg})")
+
+
+def _p(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise KDAError(f"unsupported dtype {t.dtype}")
+
+
+def make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_seqlens_host, o, S0=None, S_T=None,
+                      g_in=None, norm_w=None, y=None, g_min=-5.0, scale=1.0, qk_l2norm=True,
+                      norm_eps=1e-6, workspace=None) -> PrefillArgs:
+    """Fill the C argument struct from tensors (no validation beyond dtype mapping)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu_host = cu_seqlens_host
+    a = PrefillArgs()
+    a.num_seqs = int(cu_host.numel() - 1)
+    a.T_total, a.H, a.dk, a.dv = int(T), int(H), int(dk), int(dv)
+    a.qkv_dtype = _dtype_code(q)
+    a.cu_seqlens = cu_seqlens.data_ptr()
+    a.cu_seqlens_host = cu_host.data_ptr()
+    for name, t in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta), ("A", A),
+                    ("S0", S0), ("o", o), ("S_T", S_T), ("g_in", g_in), ("norm_w", norm_w),
+                    ("y", y)):
+        setattr(a, name, t.data_ptr() if t is not None else None)
+    a.g_min, a.scale, a.qk_l2norm, a.norm_eps = float(g_min), float(scale), int(bool(qk_l2norm)), float(norm_eps)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def prefill_workspace_size(args: PrefillArgs) -> int:
+    return int(load_library().kda_prefill_workspace_size(ctypes.byref(args)))
+
+
+def prefill_raw(args: PrefillArgs, stream=None, recurrent: bool = False):
+    lib = load_library()
+    fn = lib.kda_prefill_recurrent if recurrent else lib.kda_prefill
+    _check(fn(ctypes.byref(args), _stream(stream)), "kda_prefill_recurrent" if recurrent else "kda_prefill")
+
+
+def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
+            g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, want_state=True,
+            out=None, stream=None, recurrent=False, workspace=None):
+    """KDA chunked prefill through ``kda_prefill``.
+
+    q, k, z: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; A: [H]; cu_seqlens: int32
+    [N+1] on the device (None = one sequence).  Returns (o, S_T, y).
+    """
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = q.device
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    cu_host = cu_seqlens.to("cpu")
+    N = cu_host.numel() - 1
+    o = out["o"] if out else torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    S_T = (out["S_T"] if out else torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)) \
+        if want_state else None
+    y = None
+    if g_in is not None:
+        y = out["y"] if out else torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev)
+    args = make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_host, o, S0=S0, S_T=S_T,
+                             g_in=g_in, norm_w=norm_w, y=y, g_min=g_min, scale=scale,
+                             qk_l2norm=qk_l2norm, norm_eps=norm_eps)
+    if not recurrent:
+        need = prefill_workspace_size(args)
+        if need > 0:
+            if workspace is None or workspace.numel() * workspace.element_size() < need:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            args.workspace = workspace.data_ptr()
+            args.workspace_bytes = workspace.numel() * workspace.element_size()
+    prefill_raw(args, stream=stream, recurrent=recurrent)
+    return o, S_T, y
+
+
+def make_decode_args(q, k, v, z, beta, A, state, o=None, y=None, g_in=None, norm_w=None,
+                     slots=None, g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6) -> DecodeArgs:
+    N, H, dk = q.shape
+    a = DecodeArgs()
+    a.N, a.H, a.dk, a.dv = int(N), int(H), int(dk), int(v.shape[2])
+    a.num_slots = int(state.shape[0])
+    for name, t in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta), ("A", A),
+                    ("state", state), ("slots", slots), ("o", o), ("g_in", g_in),
+                    ("norm_w", norm_w), ("y", y)):
+        setattr(a, name, t.data_ptr() if t is not None else None)
+    a.g_min, a.scale, a.qk_l2norm, a.norm_eps = float(g_min), float(scale), int(bool(qk_l2norm)), float(norm_eps)
+    return a
+
+
+def decode_step_raw(args: DecodeArgs, stream=None):
+    _check(load_library().kda_decode_step(ctypes.byref(args), _stream(stream)), "kda_decode_step")
+
+
+def decode_step(q, k, v, z, beta, A, state, g_in=None, norm_w=None, slots=None, want_o=True,
+                g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, stream=None):
+    """One decode step through ``kda_decode_step``; ``state`` is updated in place.
+
+    Returns (o or None, y or None).
+    """
+    N, H, _ = q.shape
+    dv = v.shape[2]
+    o = torch.empty((N, H, dv), dtype=torch.bfloat16, device=q.device) if want_o else None
+    y = torch.empty((N, H, dv), dtype=torch.bfloat16, device=q.device) if g_in is not None else None
+    args = make_decode_args(q, k, v, z, beta, A, state, o=o, y=y, g_in=g_in, norm_w=norm_w,
+                            slots=slots, g_min=g_min, scale=scale, qk_l2norm=qk_l2norm,
+                            norm_eps=norm_eps)
+    decode_step_raw(args, stream)
+    return o, y
+
+
+def gate_norm(o, g_in, norm_w=None, eps=1e-6, out=None, stream=None):
+    """y = Sigmoid(g_in) * RMSNorm(o) through ``kda_gate_norm`` (rows over the last dim)."""
+    dv = o.shape[-1]
+    rows = o.numel() // dv
+    y = out if out is not None else torch.empty_like(o)
+    lib = load_library()
+    _check(lib.kda_gate_norm(_p(o), _p(g_in), _p(norm_w), ctypes.c_float(eps), _p(y),
+                             ctypes.c_long(rows), int(dv), _dtype_code(o), _stream(stream)),
+           "kda_gate_norm")
+    return y

@@ -1,0 +1,132 @@
+"""The C ABI: the library builds, loads and exports every declared symbol, the
+ctypes structs match the C layout, and host-side validation rejects bad
+arguments before anything is enqueued (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", txt)))
+
+
+def test_every_declared_symbol_is_exported(kda_lib):
+    names = declared_functions()
+    assert "kda_prefill" in names and "kda_decode_step" in names and "kda_gate_norm" in names
+    for n in names:
+        assert hasattr(kda_lib, n), f"{n} declared in kda.h but not exported"
+    import serving_kda_chunked_gated_gb300.kda as kda
+    assert sorted(kda.EXPORTED) == sorted(set(kda.EXPORTED) & set(names))
+
+
+def test_struct_layout_matches_c(tmp_path):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    prog = tmp_path / "layout.c"
+    fields_p = [f[0] for f in kda.PrefillArgs._fields_]
+    fields_d = [f[0] for f in kda.DecodeArgs._fields_]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
+             'printf("%zu %zu\\n", sizeof(kda_prefill_args), sizeof(kda_decode_args));']
+    lines += [f'printf("%zu\\n", offsetof(kda_prefill_args, {f}));' for f in fields_p]
+    lines += [f'printf("%zu\\n", offsetof(kda_decode_args, {f}));' for f in fields_d]
+    lines += ["return 0;}"]
+    prog.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", str(prog), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    sp, sd = int(out[0]), int(out[1])
+    offs = [int(x) for x in out[2:]]
+    assert sp == ctypes.sizeof(kda.PrefillArgs) and sd == ctypes.sizeof(kda.DecodeArgs)
+    assert offs[:len(fields_p)] == [getattr(kda.PrefillArgs, f).offset for f in fields_p]
+    assert offs[len(fields_p):] == [getattr(kda.DecodeArgs, f).offset for f in fields_d]
+
+
+FAKE = 0x7f0000000000  # never dereferenced: validation fails before any launch
+
+
+def _args(kda, **kw):
+    a = kda.PrefillArgs()
+    a.num_seqs, a.T_total, a.H, a.dk, a.dv, a.qkv_dtype = 1, 64, 2, 128, 128, kda.KDA_BF16
+    cu = np.array([0, 64], dtype=np.int32)
+    a.cu_seqlens = FAKE
+    a.cu_seqlens_host = cu.ctypes.data
+    for name in ("q", "k", "v", "z", "beta", "A", "o"):
+        setattr(a, name, FAKE)
+    a.g_min, a.scale, a.qk_l2norm, a.norm_eps = -5.0, 1.0, 1, 1e-6
+    for key, val in kw.items():
+        setattr(a, key, val)
+    return a, cu
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (dict(q=None), 1), (dict(A=None), 1), (dict(cu_seqlens=None), 1),
+    (dict(dk=96, dv=96), 2), (dict(dk=128, dv=64), 2), (dict(H=0), 2),
+    (dict(qkv_dtype=5), 3), (dict(q=FAKE + 4), 4), (dict(o=FAKE + 8), 4),
+    (dict(T_total=65), 5), (dict(g_in=FAKE), 1),
+])
+def test_prefill_validation(kda_lib, mutate, expect):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    a, cu = _args(kda, **mutate)
+    assert kda_lib.kda_prefill(ctypes.byref(a), None) == expect
+    assert kda_lib.kda_prefill_recurrent(ctypes.byref(a), None) == expect
+
+
+def test_prefill_seqlens_validation(kda_lib):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    a, _ = _args(kda)
+    bad = np.array([0, 40, 30, 64], dtype=np.int32)
+    a.num_seqs, a.cu_seqlens_host = 3, bad.ctypes.data
+    assert kda_lib.kda_prefill(ctypes.byref(a), None) == 5
+    bad2 = np.array([1, 64], dtype=np.int32)
+    a.num_seqs, a.cu_seqlens_host = 1, bad2.ctypes.data
+    assert kda_lib.kda_prefill(ctypes.byref(a), None) == 5
+    # f32 gate input is not accepted
+    a2, _c = _args(kda, g_in=FAKE, y=FAKE, qkv_dtype=kda.KDA_F32)
+    assert kda_lib.kda_prefill(ctypes.byref(a2), None) == 3
+    assert kda_lib.kda_prefill_workspace_size(ctypes.byref(a2)) == 0
+
+
+def test_decode_and_gate_norm_validation(kda_lib):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = kda.DecodeArgs()
+    d.N, d.H, d.dk, d.dv, d.num_slots = 4, 2, 128, 128, 4
+    for name in ("q", "k", "v", "z", "beta", "A", "state", "o"):
+        setattr(d, name, FAKE)
+    d2 = kda.DecodeArgs.from_buffer_copy(d)
+    d2.o = None
+    assert kda_lib.kda_decode_step(ctypes.byref(d2), None) == 1      # neither o nor y
+    d3 = kda.DecodeArgs.from_buffer_copy(d)
+    d3.dk = d3.dv = 64
+    assert kda_lib.kda_decode_step(ctypes.byref(d3), None) == 2
+    d4 = kda.DecodeArgs.from_buffer_copy(d)
+    d4.num_slots = 3                                                 # no slots, fewer rows than N
+    assert kda_lib.kda_decode_step(ctypes.byref(d4), None) == 2
+    d5 = kda.DecodeArgs.from_buffer_copy(d)
+    d5.state = FAKE + 12
+    assert kda_lib.kda_decode_step(ctypes.byref(d5), None) == 4
+    d6 = kda.DecodeArgs.from_buffer_copy(d)
+    d6.g_in = FAKE                                                  # g_in without y
+    assert kda_lib.kda_decode_step(ctypes.byref(d6), None) == 1
+    f = kda_lib.kda_gate_norm
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_long,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 96, 0, None) == 2
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 128, 9, None) == 3
+    assert f(None, FAKE, None, 1e-6, FAKE, 10, 128, 0, None) == 1
+    assert f(FAKE + 2, FAKE, None, 1e-6, FAKE, 10, 128, 0, None) == 4
+
+
+def test_status_strings(kda_lib):
+    kda_lib.kda_status_str.restype = ctypes.c_char_p
+    assert kda_lib.kda_status_str(0) == b"ok"
+    assert b"cu_seqlens" in kda_lib.kda_status_str(5)
+    kda_lib.kda_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in kda_lib.kda_version()

@@ -1,0 +1,104 @@
+"""Prefill on the GPU (kda_prefill through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from serving_kda_chunked_gated_gb300 import inputs as I
+from kda_testutil import TOL_O, TOL_S, f64, host, qkv_to_dev, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(kda, d, dev, recurrent=False, gate=None, s0=True, alias_state=False):
+    q, k, v = qkv_to_dev(d, dev)
+    S0 = to_dev(d["S0"], dev) if (s0 and d["S0"] is not None) else None
+    g_in = to_dev(d["g_in"], dev, True) if (d["g_in"] is not None and gate is not False) else None
+    out = None
+    if alias_state and S0 is not None:
+        out = {"o": torch.empty_like(v), "S_T": S0,
+               "y": torch.empty_like(v) if g_in is not None else None}
+    o, S_T, y = kda.prefill(q, k, v, to_dev(d["z"], dev), to_dev(d["beta"], dev), to_dev(d["A"], dev),
+                            cu_seqlens=to_dev(d["cu_seqlens"], dev), S0=S0, g_in=g_in,
+                            recurrent=recurrent, out=out)
+    torch.cuda.synchronize()
+    return o, S_T, y
+
+
+def run_oracle(d, gate=None, s0=True):
+    g = f64(d, "g_in") if gate is not False else None
+    return oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"],
+                          cu_seqlens=d["cu_seqlens"], S0=d["S0"] if s0 else None, g_in=g)
+
+
+def check(res, ref, tol_o=TOL_O, tol_s=TOL_S):
+    o, S_T, y = res
+    ro, rS, ry = ref
+    eo, es = rel(host(o), ro), rel(host(S_T), rS)
+    assert eo < tol_o, f"o rel-L2 {eo:.3e}"
+    assert es < tol_s, f"S_T rel-L2 {es:.3e}"
+    if ry is not None:
+        ey = rel(host(y), ry)
+        assert ey < tol_o, f"y rel-L2 {ey:.3e}"
+
+
+def test_tiny_fp32(kda_lib, cuda_dev):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("tiny"))
+    check(run_gpu(kda, d, cuda_dev), run_oracle(d))
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 64, 65, 300])
+def test_bf16_lengths(kda_lib, cuda_dev, T):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=T, H=2))
+    check(run_gpu(kda, d, cuda_dev), run_oracle(d))
+
+
+def test_bf16_varlen_with_empty_and_single(kda_lib, cuda_dev):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    w = I.workload("prefill_128k", T=0, H=3, S0_std=0.02)
+    d = I.make_prefill(I.workload("prefill_128k", T=400, H=3))
+    cu = np.array([0, 0, 1, 130, 130, 400], dtype=np.int32)
+    d["cu_seqlens"] = cu
+    d["S0"] = (0.02 * np.random.default_rng(1).standard_normal((5, 3, 128, 128))).astype(np.float32)
+    check(run_gpu(kda, d, cuda_dev), run_oracle(d))
+
+
+def test_in_place_state(kda_lib, cuda_dev):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=200, H=2))
+    check(run_gpu(kda, d, cuda_dev, alias_state=True), run_oracle(d))
+
+
+def test_chunked_matches_recurrent_gpu(kda_lib, cuda_dev):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=700, H=4))
+    a = run_gpu(kda, d, cuda_dev)
+    b = run_gpu(kda, d, cuda_dev, recurrent=True)
+    assert rel(host(a[0]), host(b[0])) < TOL_O
+    assert rel(host(a[1]), host(b[1])) < TOL_S
+
+
+def test_adversarial_gates(kda_lib, cuda_dev):
+    """Gates at both ends: z = +1e4 (g = g_min every step) and z = -1e4 (no decay)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=260, H=2))
+    z = d["z"]
+    z[:, 0, :64] = 1e4
+    z[:, 0, 64:] = -1e4
+    z[::3, 1, :] = 1e4
+    check(run_gpu(kda, d, cuda_dev), run_oracle(d))
+
+
+def test_full_prefill_8k_sampled(kda_lib, cuda_dev):
+    """Full 8192-token, 32-head prefill; the oracle recomputes two heads."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    w = I.workload("prefill_8k")
+    d = I.make_prefill(w)
+    o, S_T, _ = run_gpu(kda, d, cuda_dev)
+    heads = [0, 31]
+    ds = I.make_prefill(w, heads=heads)
+    ro, rS, _ = run_oracle(ds)
+    assert rel(host(o)[:, heads], ro) < TOL_O
+    assert rel(host(S_T)[:, heads], rS) < TOL_S
