@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA operator on one GB300 (one JSON line on stdout).
+
+Headline: chunked prefill of the long-context workload (T = 131072 tokens,
+H = 32 heads, dk = dv = 128, bf16 q/k/v, prefix state S0, fused output gate)
+in tokens/s, with its roofline; the batched decode step (256 sequences x 32
+heads of FP32 128x128 states, in place, fused gate) is measured in the same
+run and reported under "decode" (HBM GB/s and roofline fraction).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill_128k|prefill_8k|varlen_16]
+
+--impl reference times the CPU oracle (FP64 per-token recurrence, OpenMP over
+(sequence, head)) on the host cores, on a bounded sample of the same workload.
+Under torchrun every rank runs its own replica of the workload (no data-path
+collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (% BF16 TC peak); decode-step HBM GB/s (% of peak)"
+# algorithmic work per token per head (d = 128, chunk 64): 6 d^2 + 5 d (C+1) + C^2/3 flop
+FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 128 * 65 + 64 * 64 // 3
+TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 : bf16 ratio (GB300)
+
+WORKLOADS = {
+    "prefill_128k": dict(T=131072, H=32, d=128, S0=True, gate=True, varlen=None),
+    "prefill_8k": dict(T=8192, H=32, d=128, S0=False, gate=False, varlen=None),
+    "varlen_16": dict(T=None, H=32, d=128, S0=False, gate=False, varlen=(16, 512, 16384)),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sust=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    src="measured (MEASURED_PEAKS.json)")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------
+# inputs (seeded, synthetic, generated on the device)
+# --------------------------------------------------------------------------
+
+def make_prefill_inputs(torch, wl, dev, seed):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    H, d = wl["H"], wl["d"]
+    if wl["varlen"] is not None:
+        from serving_kda_chunked_gated_gb300.inputs import varlen_lengths
+        n, lo, hi = wl["varlen"]
+        lens = varlen_lengths(n, lo, hi, 1003)
+        cu = [0]
+        for L in lens:
+            cu.append(cu[-1] + int(L))
+    else:
+        cu = [0, wl["T"]]
+    T = cu[-1]
+
+    def unit_bf16(shape):
+        x = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True)
+        return x.to(torch.bfloat16)
+
+    inp = {
+        "q": unit_bf16((T, H, d)), "k": unit_bf16((T, H, d)),
+        "v": torch.randn((T, H, d), generator=g, device=dev).to(torch.bfloat16),
+        "z": 2.0 * torch.randn((T, H, d), generator=g, device=dev),
+        "beta": torch.sigmoid(torch.randn((T, H), generator=g, device=dev)),
+        "A": 0.5 * torch.randn((H,), generator=g, device=dev),
+        "cu_seqlens": torch.tensor(cu, dtype=torch.int32, device=dev),
+        "S0": (0.02 * torch.randn((len(cu) - 1, H, d, d), generator=g, device=dev)) if wl["S0"] else None,
+        "g_in": torch.randn((T, H, d), generator=g, device=dev).to(torch.bfloat16) if wl["gate"] else None,
+    }
+    return inp, T, len(cu) - 1
+
+
+def make_decode_inputs(torch, dev, seed, N=256, H=32, d=128):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def unit_bf16(shape):
+        x = torch.randn(shape, generator=g, device=dev)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    return {
+        "q": unit_bf16((N, H, d)), "k": unit_bf16((N, H, d)),
+        "v": torch.randn((N, H, d), generator=g, device=dev).to(torch.bfloat16),
+        "z": 2.0 * torch.randn((N, H, d), generator=g, device=dev),
+        "beta": torch.sigmoid(torch.randn((N, H), generator=g, device=dev)),
+        "A": torch.zeros((H,), device=dev),
+        "state": 0.02 * torch.randn((N, H, d, d), generator=g, device=dev),
+        "g_in": torch.randn((N, H, d), generator=g, device=dev).to(torch.bfloat16),
+    }
+
+
+def nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def kernel_traffic(kernel_file, name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source
+    still matches the hash recorded with it (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(name)
+        src = open(os.path.join(ROOT, "serving_kda_chunked_gated_gb300", "csrc", kernel_file), "rb").read()
+        if rec and rec.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return rec.get("bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+    import serving_kda_chunked_gated_gb300.kda as kda
+    from serving_kda_chunked_gated_gb300 import build as kbuild
+
+    if not os.path.exists(kda.LIB_PATH):
+        kbuild.build()
+    kda.load_library()
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pk = peaks()
+    wl = WORKLOADS[args.workload]
+    H, d = wl["H"], wl["d"]
+
+    inp, T, N = make_prefill_inputs(torch, wl, dev, seed=1234 + rank)
+    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(o) if inp["g_in"] is not None else None
+    S_T = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    cu_host = inp["cu_seqlens"].cpu()
+    pa = kda.make_prefill_args(inp["q"], inp["k"], inp["v"], inp["z"], inp["beta"], inp["A"],
+                               inp["cu_seqlens"], cu_host, o, S0=inp["S0"], S_T=S_T,
+                               g_in=inp["g_in"], y=y)
+    ws_bytes = kda.prefill_workspace_size(pa)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    pa.workspace, pa.workspace_bytes = ws.data_ptr(), ws_bytes
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        kda.prefill_raw(pa, stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    l0 = kda.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        kda.prefill_raw(pa, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = kda.launch_count() - l0
+    barrier()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_all = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_all = float(t.item())
+
+    # ---- decode step (secondary): state read + written once per step
+    dec = make_decode_inputs(torch, dev, seed=99 + rank)
+    Nd = dec["q"].shape[0]
+    od = torch.empty((Nd, H, d), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty_like(od)
+    da = kda.make_decode_args(dec["q"], dec["k"], dec["v"], dec["z"], dec["beta"], dec["A"],
+                              dec["state"], o=od, y=yd, g_in=dec["g_in"])
+    for _ in range(max(args.warmup, 3)):
+        kda.decode_step_raw(da, stream)
+    dsteps = max(args.steps, 20) * 4
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(dsteps):
+        kda.decode_step_raw(da, stream)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = d0.elapsed_time(d1) / dsteps
+    clocks = sampler.stop()
+
+    # ---- end to end: host buffers in, host buffers out, through the public call
+    e2e = None
+    if not args.no_e2e:
+        keys = [k for k in ("q", "k", "v", "z", "beta", "A", "S0", "g_in") if inp[k] is not None]
+        host_in = {k: inp[k].cpu().pin_memory() for k in keys}
+        dev_in = {k: torch.empty_like(inp[k]) for k in keys}
+        host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        host_y = torch.empty(y.shape, dtype=y.dtype).pin_memory() if y is not None else None
+        host_S = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+        pe = kda.make_prefill_args(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["z"], dev_in["beta"],
+                                   dev_in["A"], inp["cu_seqlens"], cu_host, o, S0=dev_in.get("S0"),
+                                   S_T=S_T, g_in=dev_in.get("g_in"), y=y)
+        pe.workspace, pe.workspace_bytes = ws.data_ptr(), ws_bytes
+
+        def step():
+            for k in keys:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            kda.prefill_raw(pe, stream)
+            host_o.copy_(o, non_blocking=True)
+            if y is not None:
+                host_y.copy_(y, non_blocking=True)
+            host_S.copy_(S_T, non_blocking=True)
+
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        ksteps = max(3, min(args.steps, 10))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(ksteps):
+            step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / ksteps
+        bi = sum(nbytes(host_in[k]) for k in keys)
+        bo = nbytes(host_o) + nbytes(host_y) + nbytes(host_S)
+        e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    if rank != 0:
+        return None
+
+    # algorithmic bytes of one prefill launch
+    io_per_tok_head = 3 * 2 * d + 4 * d + 4 + 2 * d + (2 * 2 * d if wl["gate"] else 0)
+    alg_bytes = T * H * io_per_tok_head + N * H * d * d * 4 * (2 if wl["S0"] else 1)
+    alg_flops = T * H * FLOP_PER_TOKEN_HEAD
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    tf32_peak = pk["bf16"] * TF32_OVER_BF16
+    dec_bytes = 2 * nbytes(dec["state"]) + sum(nbytes(dec[k]) for k in ("q", "k", "v", "z", "beta", "g_in")) \
+        + nbytes(yd) + nbytes(od)
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    path_tc = kda.prefill_workspace_size(pa) > 0 or launches > args.steps
+    res = {
+        "metric": METRIC,
+        "value": world * T / (ms_all * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_all,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "tf32" if path_tc else "f32",
+        "data": "synthetic (seeded, generated on the device)",
+        "config": {"workload": args.workload, "tokens": T, "num_seqs": N, "H": H, "dk": d, "dv": d,
+                   "qkv": "bf16", "S0": wl["S0"], "fused_gate": wl["gate"], "qk_l2norm": True,
+                   "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm"], "traffic": kernel_traffic("prefill_tc.cu", "prefill"),
+                     "peak_source": pk["src"] + " hbm_gbs (burst copy)",
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "tensor": {"achieved_tflops": alg_flops / (ms * 1e-3) / 1e12,
+                                "peak_tf32_tflops": tf32_peak,
+                                "frac_of_tf32": alg_flops / (ms * 1e-3) / 1e12 / tf32_peak,
+                                "frac_of_bf16": alg_flops / (ms * 1e-3) / 1e12 / pk["bf16"]}},
+        "decode": {"workload": "decode_256", "ms_per_step": dec_ms, "value": dec_gbs, "unit": "GB/s",
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                                "frac": dec_gbs / pk["hbm"],
+                                "traffic": kernel_traffic("decode.cu", "decode"),
+                                "algorithmic_bytes_per_launch": dec_bytes}},
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    return res
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle, timed on the host cores
+# --------------------------------------------------------------------------
+
+def _oracle_sample(workload, T_s, seed_offset=0):
+    import numpy as np
+    from serving_kda_chunked_gated_gb300 import inputs as I
+    name = workload if workload != "varlen_16" else "prefill_8k"
+    w = I.workload(name, T=T_s, varlen=None)
+    d = I.make_prefill(w)
+    f = lambda x: I.bf16_to_f32(x).astype(np.float64)
+    return d, (f(d["q"]), f(d["k"]), f(d["v"]), d["z"].astype(np.float64), d["beta"].astype(np.float64),
+               d["A"].astype(np.float64)), (f(d["g_in"]) if d["g_in"] is not None else None)
+
+
+def cpu_baseline(workload, budget_s=12.0, T_s=4096):
+    import oracle
+    oracle.build()
+    d, (q, k, v, z, beta, A), g_in = _oracle_sample(workload, T_s)
+    H = q.shape[1]
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 50:
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, z, beta, A, S0=d["S0"], g_in=g_in)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return {"value": reps * T_s / t_total, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} x ({T_s} tokens x {H} heads, d=128, same distributions as {workload}); "
+                      f"FP64 per-token recurrence, OpenMP over heads; {t_total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    T_s = 4096
+    d, (q, k, v, z, beta, A), g_in = _oracle_sample(args.workload, T_s)
+    for _ in range(args.warmup):
+        oracle.prefill(q, k, v, z, beta, A, S0=d["S0"], g_in=g_in)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, z, beta, A, S0=d["S0"], g_in=g_in)
+        times.append(time.perf_counter() - t0)
+    step = sum(times) / len(times)
+    val = T_s / step
+    wl = WORKLOADS[args.workload]
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "tokens": wl["T"], "H": wl["H"], "dk": 128, "dv": 128,
+                   "sample_tokens_per_step": T_s},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{T_s} tokens x {q.shape[1]} heads per step of {args.workload}"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill_128k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        torch.distributed.init_process_group("nccl")
+    res = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -175,6 +175,11 @@ const char* kda_status_str(kda_status s);
 /* Text of the last CUDA error seen by this thread inside the library. */
 const char* kda_last_error_string(void);
 
+/* Number of kernel launches this library has enqueued from the calling host
+ * thread since the thread first called into it (a monotone counter, for
+ * accounting launches inside a timed region). */
+uint64_t kda_launch_count(void);
+
 /* Library build description (architecture, version). */
 const char* kda_version(void);
 

@@ -17,6 +17,12 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 }  // namespace kda
 
 static thread_local char g_last_error[256] = "no error";
+static thread_local uint64_t g_launches = 0;
+
+namespace kda {
+// called by every launch wrapper once per kernel enqueued
+void count_launches(int n) { g_launches += (uint64_t)n; }
+}  // namespace kda
 
 static kda_status cuda_fail(cudaError_t e) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -43,6 +49,8 @@ const char* kda_status_str(kda_status s) {
 }
 
 const char* kda_last_error_string(void) { return g_last_error; }
+
+uint64_t kda_launch_count(void) { return g_launches; }
 
 const char* kda_version(void) { return "kda-gb300 0.1 (sm_103a; tcgen05 tf32 chunked prefill)"; }
 

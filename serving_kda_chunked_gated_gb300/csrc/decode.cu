@@ -130,6 +130,7 @@ cudaError_t launch_decode_step(const kda_decode_args& a, cudaStream_t stream) {
     const long blocks = (long)a.N * a.H;
     if (blocks == 0) return cudaSuccess;
     decode_step_kernel<<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

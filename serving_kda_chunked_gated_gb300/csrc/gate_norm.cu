@@ -43,6 +43,7 @@ template <int DV>
 static cudaError_t launch_gn(const void* o, const void* g, const float* w, float eps, void* y,
                              long rows, bool bf16, cudaStream_t s) {
     const unsigned blocks = (unsigned)((rows + 7) / 8);
+    count_launches(1);
     if (bf16) gate_norm_kernel<DV, true><<<blocks, 256, 0, s>>>(o, g, w, eps, y, rows);
     else gate_norm_kernel<DV, false><<<blocks, 256, 0, s>>>(o, g, w, eps, y, rows);
     return cudaGetLastError();

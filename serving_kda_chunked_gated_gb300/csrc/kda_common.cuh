@@ -10,6 +10,9 @@
 
 namespace kda {
 
+// launch accounting (api.cu): every launch wrapper reports the kernels it enqueued
+void count_launches(int n);
+
 // Logistic function through the hardware exp2 / fast-divide path.
 KDA_DEV float sigmoidf_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 

@@ -121,6 +121,7 @@ prefill_recurrent_kernel(kda_prefill_args a) {
 template <int D, bool BF16>
 static cudaError_t launch_rec(const kda_prefill_args& a, cudaStream_t s) {
     prefill_recurrent_kernel<D, BF16><<<(unsigned)((long)a.num_seqs * a.H), 256, 0, s>>>(a);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
-            "kda_version"]
+            "kda_version", "kda_launch_count"]
 
 _vp = ctypes.c_void_p
 
@@ -84,8 +84,14 @@ def load_library(path: str = LIB_PATH):
     lib.kda_status_str.restype = ctypes.c_char_p
     lib.kda_last_error_string.restype = ctypes.c_char_p
     lib.kda_version.restype = ctypes.c_char_p
+    lib.kda_launch_count.restype = ctypes.c_uint64
     _lib = lib
     return lib
+
+
+def launch_count() -> int:
+    """Kernel launches enqueued by this library from the calling thread so far."""
+    return int(load_library().kda_launch_count())
 
 
 def _check(status: int, what: str):
