@@ -185,7 +185,7 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
         need = prefill_workspace_size(args)
         if need > 0:
             if workspace is None or workspace.numel() * workspace.element_size() < need:
-                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+                workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
             args.workspace = workspace.data_ptr()
             args.workspace_bytes = workspace.numel() * workspace.element_size()
     prefill_raw(args, stream=stream, recurrent=recurrent)

@@ -102,3 +102,52 @@ def test_full_prefill_8k_sampled(kda_lib, cuda_dev):
     ro, rS, _ = run_oracle(ds)
     assert rel(host(o)[:, heads], ro) < TOL_O
     assert rel(host(S_T)[:, heads], rS) < TOL_S
+
+
+def test_full_prefill_128k_sampled_and_deterministic(kda_lib, cuda_dev):
+    """Long-context prefill (131072 tokens, 32 heads, prefix state, fused gate):
+    one head checked against the oracle; two runs bit-identical; no bounded
+    wait gave up (the workspace error word stays 0)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    w = I.workload("prefill_128k")
+    d = I.make_prefill(w)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    args = dict(cu_seqlens=to_dev(d["cu_seqlens"], cuda_dev), S0=to_dev(d["S0"], cuda_dev),
+                g_in=to_dev(d["g_in"], cuda_dev, True))
+    z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
+    ws = torch.zeros(4096, dtype=torch.uint8, device=cuda_dev)
+    o, S_T, y = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
+    o2, S_T2, y2 = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert torch.equal(o, o2) and torch.equal(S_T, S_T2) and torch.equal(y, y2)
+    del q, k, v, z, beta, args
+    heads = [5]
+    ds = I.make_prefill(w, heads=heads)
+    ro, rS, ry = run_oracle(ds)
+    assert rel(host(o[:, heads]), ro) < TOL_O
+    assert rel(host(y[:, heads]), ry) < TOL_O
+    assert rel(host(S_T[:, heads]), rS) < TOL_S
+
+
+def test_full_varlen_16_sampled(kda_lib, cuda_dev):
+    """Packed 16-sequence prefill (lengths 512..16384); two heads checked for
+    every sequence; the packed result equals per-sequence calls bit for bit."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    w = I.workload("varlen_16")
+    d = I.make_prefill(w)
+    o, S_T, _ = run_gpu(kda, d, cuda_dev)
+    heads = [0, 31]
+    ds = I.make_prefill(w, heads=heads)
+    ro, rS, _ = run_oracle(ds)
+    assert rel(host(o)[:, heads], ro) < TOL_O
+    assert rel(host(S_T)[:, heads], rS) < TOL_S
+    cu = d["cu_seqlens"]
+    for n in (0, 7, 15):
+        s, e = int(cu[n]), int(cu[n + 1])
+        sub = dict(d)
+        for key in ("q", "k", "v", "z", "beta"):
+            sub[key] = np.ascontiguousarray(d[key][s:e])
+        sub["cu_seqlens"] = np.array([0, e - s], dtype=np.int32)
+        o1, S1, _ = run_gpu(kda, sub, cuda_dev)
+        assert torch.equal(o1, o[s:e]) and torch.equal(S1[0], S_T[n])
