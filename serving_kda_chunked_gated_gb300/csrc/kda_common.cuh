@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/kda.h"
+#include "kda.h"   // include/ is on the include path
 
 #define KDA_DEV __device__ __forceinline__
 
