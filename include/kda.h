@@ -111,6 +111,32 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* args);
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 
 /*
+ * kda_prefill for callers that cannot allocate device memory.  (Library
+ * plumbing: the KDA pages have no counterpart of this entry point.)
+ *
+ * Some callers cannot call cudaMalloc at all -- for example a serving engine
+ * or plugin host that reserves all device memory for its own pool up front and
+ * forbids allocation while requests run -- and so cannot provide the
+ * workspace kda_prefill asks for.  This entry point takes the same arguments
+ * but ignores args->workspace / args->workspace_bytes and uses instead a fixed
+ * array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's own device memory
+ * (every GPU that loads the library holds it until the process exits).  It
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - Calls whose scratch requirement (kda_prefill_workspace_size) exceeds
+ *    KDA_NOALLOC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE (the
+ *    message is in kda_last_error_string()).
+ *  - All calls share the one array; it keeps the previous call's contents and
+ *    each call clears what must start at zero (with cudaMemsetAsync on the
+ *    caller's stream).  Calls that overlap on the GPU (different streams with
+ *    no ordering between them) race on the array: serialise them.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ * Inputs and outputs are the caller's, exactly as for kda_prefill.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES 4096
+kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
+
+/*
  * The same operator as kda_prefill, always evaluated by the per-token
  * recurrence on CUDA cores (one CTA per sequence and head, the state held in
  * registers).  Same arguments, layouts, validation and status codes as

@@ -12,6 +12,8 @@ cudaError_t launch_gate_norm(const void* o, const void* g, const float* w, float
                              long rows, int dv, bool bf16, cudaStream_t s);
 cudaError_t launch_prefill_recurrent(const kda_prefill_args& a, cudaStream_t s);
 bool prefill_tc_supported(const kda_prefill_args& a);
+size_t prefill_noalloc_scratch_needed(const kda_prefill_args& a);
+cudaError_t launch_prefill_tc_noalloc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_tc_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 }  // namespace kda
@@ -101,6 +103,23 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
     } else {
         e = kda::launch_prefill_recurrent(*a, s);
     }
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+kda_status kda_prefill_noalloc(const kda_prefill_args* a, void* stream) {
+    kda_status st = validate_prefill(a);
+    if (st != KDA_OK) return st;
+    const size_t need = kda::prefill_noalloc_scratch_needed(*a);
+    if (need > KDA_NOALLOC_SCRATCH_BYTES) {
+        snprintf(g_last_error, sizeof(g_last_error),
+                 "kda_prefill_noalloc: this call needs %zu bytes of scratch, the fixed array holds %d",
+                 need, KDA_NOALLOC_SCRATCH_BYTES);
+        return KDA_ERR_WORKSPACE;
+    }
+    if (a->num_seqs == 0) return KDA_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::prefill_tc_supported(*a) ? kda::launch_prefill_tc_noalloc(*a, s)
+                                                  : kda::launch_prefill_recurrent(*a, s);
     return e == cudaSuccess ? KDA_OK : cuda_fail(e);
 }
 

@@ -25,6 +25,8 @@
 // tf32 (nearest) when staged; the gate, cumulative decays, the triangular
 // solve and the state carry stay FP32 (the state lives in TMEM in FP32 across
 // chunks and is only rounded for its copy used as an MMA operand).
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "tcgen05.cuh"
 
@@ -530,6 +532,53 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s) {
     tcp::prefill_tc_kernel<<<grid, tcp::NT, tcp::SMEM_BYTES, s>>>(a, reinterpret_cast<int*>(a.workspace));
     count_launches(1);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (kda_prefill_noalloc): the scratch this kernel needs
+// lives in a fixed array of the library's own device memory instead of a
+// caller-provided workspace.  Every GPU that loads the library holds the
+// array until the process exits; all calls share it.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device with that device current (in host code the symbol name is only a
+// host-side stand-in, never a device address).
+static cudaError_t noalloc_scratch_address(void** out) {
+    static std::mutex mu;
+    static void* addr[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+size_t prefill_noalloc_scratch_needed(const kda_prefill_args& a) {
+    return prefill_tc_supported(a) ? prefill_tc_workspace_size(a) : 0;
+}
+
+cudaError_t launch_prefill_tc_noalloc(const kda_prefill_args& a, cudaStream_t s) {
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    const size_t need = prefill_tc_workspace_size(a);
+    // the error word must start at zero; the array keeps the previous call's contents
+    e = cudaMemsetAsync(scratch, 0, need, s);
+    if (e != cudaSuccess) return e;
+    kda_prefill_args b = a;
+    b.workspace = scratch;
+    b.workspace_bytes = KDA_NOALLOC_SCRATCH_BYTES;
+    return launch_prefill_tc(b, s);
 }
 
 }  // namespace kda

@@ -23,7 +23,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
-            "kda_version", "kda_launch_count"]
+            "kda_version", "kda_launch_count", "kda_prefill_noalloc"]
 
 _vp = ctypes.c_void_p
 
@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
     lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+    lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_recurrent.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
     lib.kda_prefill_recurrent.restype = ctypes.c_int
     lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
@@ -145,6 +147,13 @@ def make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_seqlens_host, o, S0=No
         a.workspace = workspace.data_ptr()
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     return a
+
+
+def prefill_noalloc_raw(args: PrefillArgs, stream=None):
+    """``kda_prefill_noalloc``: for callers that cannot allocate device memory.
+    The workspace fields of ``args`` are ignored; the library's fixed device
+    scratch array is used instead.  Calls on unordered streams race on it."""
+    _check(load_library().kda_prefill_noalloc(ctypes.byref(args), _stream(stream)), "kda_prefill_noalloc")
 
 
 def prefill_workspace_size(args: PrefillArgs) -> int:
