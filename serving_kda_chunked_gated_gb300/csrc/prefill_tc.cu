@@ -20,11 +20,20 @@
 // the only exchange is the per-row sum of squares for the RMSNorm of the
 // fused output gate (over distributed shared memory).
 //
+// Data movement: each chunk's q, k, z tiles (64 x 128) and this CTA's v and
+// g_in tiles (64 x 64) arrive by TMA bulk tensor copies into shared memory,
+// issued one chunk ahead (q/k/z as soon as the previous chunk's first MMA has
+// consumed their buffer, v/g_in after the previous chunk's epilogue), so the
+// CUDA-core prologue reads shared memory only.
+//
 // Precision: every contraction runs as tcgen05 kind::tf32 (the 16x16 Gram
 // sub-blocks as mma.sync tf32) with FP32 accumulation; operands are rounded to
 // tf32 (nearest) when staged; the gate, cumulative decays, the triangular
 // solve and the state carry stay FP32 (the state lives in TMEM in FP32 across
 // chunks and is only rounded for its copy used as an MMA operand).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -39,28 +48,41 @@ constexpr int NE = 64;    // value columns per CTA
 constexpr int NT = 128;   // threads per CTA
 constexpr int QS = 132;   // padded row stride (floats) of the scaled q/k tiles
 constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
+constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
 
 // shared memory map (offsets from a 1024-aligned base)
-constexpr int SOP_BYTES = NE * D * 4;                 // S operand, SW128 [e][d]      32 KB
-constexpr int BPRE_BYTES = (NE + D) * C * 4;          // [V | Gamma K]^T, SW128 [n][t] 48 KB
-constexpr int TILE_BYTES = C * QS * 4;                // one scaled q/k tile           33 KB
+constexpr int SOP_BYTES = NE * D * 4;                 // S operand, SW128 [e][d]            32 KB
+constexpr int RB_BYTES = 65536;                       // raw q,k,z | Gram tiles | [V|GK]^T  64 KB
+constexpr int TILE_BYTES = C * QS * 4;                // one scaled q/k tile                33 KB
+constexpr int VG_BYTES = 2 * C * NE * 2;              // raw v, g_in halves (bf16, swizzled) 16 KB
 constexpr int OFF_SOP = 0;
-constexpr int OFF_BPRE = OFF_SOP + SOP_BYTES;
-constexpr int OFF_QH = OFF_BPRE + BPRE_BYTES;         // q * exp(G - G_subchunk_start)
+constexpr int OFF_RB = OFF_SOP + SOP_BYTES;
+constexpr int OFF_RAWQ = OFF_RB;                      // [C][D] bf16
+constexpr int OFF_RAWK = OFF_RB + C * D * 2;          // [C][D] bf16
+constexpr int OFF_RAWZ = OFF_RB + 2 * C * D * 2;      // [C][D] f32
+constexpr int OFF_AQK = OFF_RB;                       // Gram tiles
+constexpr int OFF_AKK = OFF_RB + C * AS * 4;
+constexpr int OFF_BPRE = OFF_RB;                      // [V | Gamma K]^T, SW128 [n][t]
+constexpr int OFF_QH = OFF_RB + RB_BYTES;             // q * exp(G - G_subchunk_start)
 constexpr int OFF_KR = OFF_QH + TILE_BYTES;           // k * exp(G - G_subchunk_start)
 constexpr int OFF_KH = OFF_KR + TILE_BYTES;           // k * exp(G_subchunk_end - G)
 constexpr int OFF_VOP = OFF_KR;                       // V' operand [e][t] (aliases KR)
-constexpr int OFF_AQK = OFF_BPRE;                     // Gram tiles (alias B_pre)
-constexpr int OFF_AKK = OFF_BPRE + C * AS * 4;
-constexpr int OFF_SMALL = OFF_KH + TILE_BYTES;
+constexpr int OFF_RAWV = OFF_KH + TILE_BYTES;         // [C][NE] bf16, 128-B swizzle
+constexpr int OFF_RAWG = OFF_RAWV + C * NE * 2;       // [C][NE] bf16, 128-B swizzle
+constexpr int OFF_SMALL = OFF_RAWV + VG_BYTES;
 // small region (floats)
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_ROWSQ = SM_GAM + D,
-              SM_FLOATS = SM_ROWSQ + 2 * C;
-constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 /*mbarrier, tmem base*/ + 1024 /*align*/;
+              SM_CTAB = SM_ROWSQ + 2 * C, SM_FLOATS = SM_CTAB + NPAIR * D;
+constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 /*mbarriers, tmem base*/ + 1024 /*align*/;
 static_assert(OFF_VOP % 1024 == 0 && OFF_BPRE % 1024 == 0, "SW128 operands need 1024-B alignment");
-static_assert(2 * C * AS * 4 <= BPRE_BYTES, "Gram tiles must fit in the B_pre region");
+static_assert(OFF_RAWV % 1024 == 0 && OFF_RAWG % 1024 == 0, "128-B swizzled TMA tiles need 1024-B alignment");
+static_assert(2 * C * AS * 4 <= RB_BYTES && (NE + D) * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES,
+              "region RB holds the raw tiles, the Gram tiles and [V|GK]^T in turn");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;   // one chunk of q, k, z
+constexpr uint32_t BYTES_V = C * NE * 2;                    // one chunk of the v (or g_in) half
 
 // TMEM columns
 constexpr uint32_t TM_D = 0;      // 192 cols: [U;U_o] -> [V';O] (0..63), [W;P Gamma K] -> A1 (64..191)
@@ -81,14 +103,26 @@ TC_DEV void st_cluster_f32(uint32_t addr, float v) {
 TC_DEV void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// byte offset of bf16 element (row, col) in a [rows][64] tile written by TMA with the 128-B swizzle
+TC_DEV uint32_t sw128_bf16(int row, int col) {
+    return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
-prefill_tc_kernel(kda_prefill_args a, int* err) {
+prefill_tc_kernel(kda_prefill_args a, int* err,
+                  const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_g) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sSop = sm + OFF_SOP;
     uint8_t* sBpre = sm + OFF_BPRE;
     uint8_t* sVop = sm + OFF_VOP;
+    const uint16_t* sRawQ = reinterpret_cast<const uint16_t*>(sm + OFF_RAWQ);
+    const uint16_t* sRawK = reinterpret_cast<const uint16_t*>(sm + OFF_RAWK);
+    const float* sRawZ = reinterpret_cast<const float*>(sm + OFF_RAWZ);
+    const uint8_t* sRawV = sm + OFF_RAWV;
+    const uint8_t* sRawG = sm + OFF_RAWG;
     float* sQ = reinterpret_cast<float*>(sm + OFF_QH);
     float* sKr = reinterpret_cast<float*>(sm + OFF_KR);
     float* sK = reinterpret_cast<float*>(sm + OFF_KH);
@@ -103,8 +137,11 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
     float* s_expCE = fs + SM_EXPCE;  // [4][D] exp(G_C - G at sub-chunk end)
     float* s_gam = fs + SM_GAM;      // [D]    exp(G_C)
     float* s_rowsq = fs + SM_ROWSQ;  // [2][C] peer's row sums of squares (by chunk parity)
+    float* s_ctab = fs + SM_CTAB;    // [NPAIR][D] exp(G_start(a) - G_end(b)), b < a; 1/tau_a for b = a
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 1);
+    uint64_t* bar_in = mbar + 1;
+    uint64_t* bar_vg = mbar + 2;
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 3);
 
     const int r = blockIdx.x;          // value half == cluster rank
     const int h = blockIdx.y;
@@ -112,26 +149,46 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
-    const uint16_t* qp = reinterpret_cast<const uint16_t*>(a.q);
-    const uint16_t* kp = reinterpret_cast<const uint16_t*>(a.k);
-    const uint16_t* vp = reinterpret_cast<const uint16_t*>(a.v);
     const float eA = __expf(a.A[h]);
     const bool gate = a.g_in != nullptr;
+    const uint32_t bytes_vg = gate ? 2 * BYTES_V : BYTES_V;
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
-    if (tid == 0) { tc::mbar_init(mbar, 1); tc::mbar_fence_init(); }
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::mbar_init(bar_in, 1);
+        tc::mbar_init(bar_vg, 1);
+        tc::mbar_fence_init();
+        tc::tma_prefetch_desc(&tm_q);
+        tc::tma_prefetch_desc(&tm_k);
+        tc::tma_prefetch_desc(&tm_z);
+        tc::tma_prefetch_desc(&tm_v);
+        if (gate) tc::tma_prefetch_desc(&tm_g);
+        if (t_begin < t_end) {
+            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
+            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, h * D, t_begin, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, h * D, t_begin, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, h * D, t_begin, bar_in);
+            tc::mbar_arrive_expect_tx(bar_vg, bytes_vg);
+            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, h * D + NE * r, t_begin, bar_vg);
+            if (gate) tc::tma_load_2d(sm + OFF_RAWG, &tm_g, h * D + NE * r, t_begin, bar_vg);
+        }
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t T0 = *tbase_ptr;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t phase = 0;
+    uint32_t ph_mma = 0, ph_in = 0, ph_vg = 0;
     bool timed_out = false;
     auto mma_wait = [&]() {
-        if (!tc::mbar_wait_bounded(mbar, phase, 1u << 22)) timed_out = true;
-        phase ^= 1u;
+        if (!tc::mbar_wait_bounded(mbar, ph_mma, 1u << 22)) timed_out = true;
+        ph_mma ^= 1u;
         tc::fence_after_sync();
     };
+    // write strengths of the next chunk, prefetched into a register one chunk ahead
+    float beta_next = 0.f;
+    if (tid < C && t_begin + tid < t_end) beta_next = a.beta[(size_t)(t_begin + tid) * H + h];
 
     // ---- initial state -> TMEM master copy and the tf32 operand copy
     {
@@ -156,17 +213,23 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
     for (int c0 = t_begin; c0 < t_end; c0 += C) {
         const int nc = min(C, t_end - c0);
         const int par = ((c0 - t_begin) / C) & 1;
+        const bool has_next = c0 + C < t_end;
 
-        // ---- 1a. write strengths and q/k L2 norms (warp w: tokens 16w..16w+15)
-        if (tid < C) s_beta[tid] = tid < nc ? a.beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        if (tid < C) {
+            s_beta[tid] = beta_next;
+            beta_next = (c0 + C + tid < t_end) ? a.beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
+        }
+        if (!tc::mbar_wait_bounded(bar_in, ph_in, 1u << 22)) timed_out = true;
+        ph_in ^= 1u;
+
+        // ---- 1a. q/k L2 norms (warp w: tokens 16w..16w+15) from the staged tiles
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
             const int t = warp * 16 + i;
             float sq = 0.f, sk = 0.f;
             if (t < nc) {
-                const size_t base = ((size_t)(c0 + t) * H + h) * D + 4 * lane;
-                const uint2 qa = *reinterpret_cast<const uint2*>(qp + base);
-                const uint2 ka = *reinterpret_cast<const uint2*>(kp + base);
+                const uint2 qa = *reinterpret_cast<const uint2*>(sRawQ + t * D + 4 * lane);
+                const uint2 ka = *reinterpret_cast<const uint2*>(sRawK + t * D + 4 * lane);
                 const float q0 = __uint_as_float(qa.x << 16), q1 = __uint_as_float(qa.x & 0xffff0000u),
                             q2 = __uint_as_float(qa.y << 16), q3 = __uint_as_float(qa.y & 0xffff0000u);
                 const float k0 = __uint_as_float(ka.x << 16), k1 = __uint_as_float(ka.x & 0xffff0000u),
@@ -186,8 +249,9 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
         // ---- 1b. gate, sub-chunk-relative decay factors, scaled q/k tiles (thread = channel d)
         {
             const int d = tid;
+            float tau[4];
             float pre = 1.f;                       // exp(G at the start of sub-chunk b)
-#pragma unroll 1
+#pragma unroll
             for (int b = 0; b < 4; ++b) {
                 float al[16], kv[16];
                 float F1 = 1.f;
@@ -196,10 +260,9 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
                     const int t = 16 * b + i;
                     float alpha = 1.f, q = 0.f, k = 0.f;
                     if (t < nc) {
-                        const size_t e = ((size_t)(c0 + t) * H + h) * D + d;
-                        alpha = __expf(log_decay(a.z[e], eA, a.g_min));
-                        q = bf16_to_f(qp[e]) * s_rq[t];
-                        k = bf16_to_f(kp[e]) * s_rk[t];
+                        alpha = __expf(log_decay(sRawZ[t * D + d], eA, a.g_min));
+                        q = bf16_to_f(sRawQ[t * D + d]) * s_rq[t];
+                        k = bf16_to_f(sRawK[t * D + d]) * s_rk[t];
                     }
                     F1 *= alpha;                   // exp(G_t - G_start(b))
                     al[i] = alpha;
@@ -213,6 +276,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
                     sK[(16 * b + i) * QS + d] = kv[i] * F2;
                     F2 *= al[i];
                 }
+                tau[b] = F1;
                 s_tau[b * D + d] = F1;
                 s_expS[b * D + d] = pre;
                 pre *= F1;
@@ -220,54 +284,79 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
             s_gam[d] = pre;
             float suf = 1.f;
 #pragma unroll
-            for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= s_tau[b * D + d]; }
+            for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= tau[b]; }
+            // factor joining the row reference (start of sub-chunk a) and the key
+            // reference (end of sub-chunk b): exp(G_start(a) - G_end(b))
+#pragma unroll
+            for (int aa = 0; aa < 4; ++aa) {
+#pragma unroll
+                for (int bb = 0; bb <= aa; ++bb) {
+                    float cf = 1.f;
+                    if (aa == bb) cf = __fdividef(1.f, tau[aa]);
+                    else {
+#pragma unroll
+                        for (int m = bb + 1; m < aa; ++m) cf *= tau[m];
+                    }
+                    s_ctab[(aa * (aa + 1) / 2 + bb) * D + d] = cf;
+                }
+            }
         }
-        __syncthreads();
+        __syncthreads();   // the raw q/k/z tiles are dead from here on
 
-        // ---- 2. Gram sub-blocks with mma.sync (tf32): warp w -> QK row block w, KK row block 3-w
+        // ---- 2. Gram sub-blocks with mma.sync (tf32).  Warp w owns the QK blocks of
+        //         row block w and the KK blocks of row block 3-w: five 16x16 blocks,
+        //         ten independent accumulator chains.
         {
             const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {
-                const int ab = pass == 0 ? warp : 3 - warp;
-                const float* Arow = pass == 0 ? sQ : sKr;
-                float* Out = pass == 0 ? sAqk : sAkk;
-#pragma unroll 1
-                for (int b = 0; b <= ab; ++b) {
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-                    for (int ks = 0; ks < 16; ++ks) {
-                        const int k0 = 8 * ks + t4, k1 = k0 + 4;
-                        // per-channel factor joining the two references: exp(G_start(ab) - G_end(b))
-                        float c0f, c1f;
-                        if (ab == b) {
-                            c0f = __fdividef(1.f, s_tau[b * D + k0]);
-                            c1f = __fdividef(1.f, s_tau[b * D + k1]);
-                        } else {
-                            c0f = 1.f; c1f = 1.f;
-                            for (int m = b + 1; m < ab; ++m) { c0f *= s_tau[m * D + k0]; c1f *= s_tau[m * D + k1]; }
-                        }
-                        const int ra = 16 * ab + g;
-                        float af[4] = {tc::to_tf32(Arow[ra * QS + k0]), tc::to_tf32(Arow[(ra + 8) * QS + k0]),
-                                       tc::to_tf32(Arow[ra * QS + k1]), tc::to_tf32(Arow[(ra + 8) * QS + k1])};
+            const int a0 = warp, a1 = 3 - warp, n0 = warp + 1;
+            float acc[5][2][4];
 #pragma unroll
-                        for (int nh = 0; nh < 2; ++nh) {
-                            const int j = 16 * b + 8 * nh + g;
-                            float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
-                            tc::mma_m16n8k8_tf32(acc[nh], af, bfr);
-                        }
-                    }
+            for (int it = 0; it < 5; ++it)
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
+            const int rq = 16 * a0 + g, rk = 16 * a1 + g;
+#pragma unroll 2
+            for (int ks = 0; ks < 16; ++ks) {
+                const int k0 = 8 * ks + t4, k1 = k0 + 4;
+                const float aq[4] = {tc::to_tf32(sQ[rq * QS + k0]), tc::to_tf32(sQ[(rq + 8) * QS + k0]),
+                                     tc::to_tf32(sQ[rq * QS + k1]), tc::to_tf32(sQ[(rq + 8) * QS + k1])};
+                const float ak[4] = {tc::to_tf32(sKr[rk * QS + k0]), tc::to_tf32(sKr[(rk + 8) * QS + k0]),
+                                     tc::to_tf32(sKr[rk * QS + k1]), tc::to_tf32(sKr[(rk + 8) * QS + k1])};
+#pragma unroll
+                for (int it = 0; it < 5; ++it) {
+                    const bool p1 = it >= n0;
+                    const int aa = p1 ? a1 : a0;
+                    const int bb = p1 ? it - n0 : it;
+                    const float* ct = s_ctab + (aa * (aa + 1) / 2 + bb) * D;
+                    const float c0f = ct[k0], c1f = ct[k1];
+                    const float af[4] = {p1 ? ak[0] : aq[0], p1 ? ak[1] : aq[1],
+                                         p1 ? ak[2] : aq[2], p1 ? ak[3] : aq[3]};
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
+                        const int j = 16 * bb + 8 * nh + g;
+                        const float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
+                        tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
+                    }
+                }
+            }
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int I = 16 * ab + g + (q4 >= 2 ? 8 : 0);
-                            const int J = 16 * b + 8 * nh + 2 * t4 + (q4 & 1);
-                            float val = acc[nh][q4];
-                            if (pass == 0) { if (J > I) val = 0.f; }
-                            else { val = (J >= I) ? 0.f : val * s_beta[I]; }
-                            Out[I * AS + J] = val;
-                        }
+            for (int it = 0; it < 5; ++it) {
+                const bool p1 = it >= n0;
+                const int aa = p1 ? a1 : a0;
+                const int bb = p1 ? it - n0 : it;
+                float* Out = p1 ? sAkk : sAqk;
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int I = 16 * aa + g + (q4 >= 2 ? 8 : 0);
+                        const int J = 16 * bb + 8 * nh + 2 * t4 + (q4 & 1);
+                        float val = acc[it][nh][q4];
+                        if (!p1) { if (J > I) val = 0.f; }
+                        else { val = (J >= I) ? 0.f : val * s_beta[I]; }
+                        Out[I * AS + J] = val;
                     }
                 }
             }
@@ -275,19 +364,31 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
         __syncthreads();
 
         // ---- 3. UT solve: rows of T = (I + A_kk)^{-1} (threads 0..63) and of
-        //         A_qk (I + A_kk)^{-1} (threads 64..127), then scale columns by beta
+        //         A_qk (I + A_kk)^{-1} (threads 64..127), then scale columns by beta.
+        //         Row i of either has zeros beyond column i, so a warp whose rows
+        //         are all below 32 skips the upper half of the sweep.
         {
             const int i = tid & 63;
             const bool isP = tid >= 64;
+            const int kmax = (warp & 1) ? C - 1 : 31;
             float x[C];
 #pragma unroll
             for (int j = 0; j < C; ++j) x[j] = isP ? (j <= i ? sAqk[i * AS + j] : 0.f) : (j == i ? 1.f : 0.f);
             // x (I + A) = rhs, A strictly lower: x_j = rhs_j - sum_{k>j} x_k A[k][j]
 #pragma unroll
             for (int kk = C - 1; kk >= 1; --kk) {
-                const float xk = x[kk];
+                if (kk <= kmax) {
+                    const float xk = x[kk];
+                    const float* row = sAkk + kk * AS;
 #pragma unroll
-                for (int j = 0; j < kk; ++j) x[j] = fmaf(-xk, sAkk[kk * AS + j], x[j]);
+                    for (int j4 = 0; j4 < kk; j4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(row + j4);
+                        x[j4] = fmaf(-xk, a4.x, x[j4]);
+                        if (j4 + 1 < kk) x[j4 + 1] = fmaf(-xk, a4.y, x[j4 + 1]);
+                        if (j4 + 2 < kk) x[j4 + 2] = fmaf(-xk, a4.z, x[j4 + 2]);
+                        if (j4 + 3 < kk) x[j4 + 3] = fmaf(-xk, a4.w, x[j4 + 3]);
+                    }
+                }
             }
             float v[16];
 #pragma unroll
@@ -297,19 +398,22 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
                 tc::tmem_st16(T0 + TM_A2 + lane_base + c, v);
             }
         }
-        __syncthreads();   // Gram tiles (aliasing B_pre) are dead from here on
+        __syncthreads();   // Gram tiles are dead from here on
+        if (!tc::mbar_wait_bounded(bar_vg, ph_vg, 1u << 22)) timed_out = true;
+        ph_vg ^= 1u;
 
         // ---- 4. B_pre = [V_half | Gamma K]^T (smem) and A3 = (K gamma_C / Gamma)^T (TMEM)
         {
             if (tid < NE) {
                 const int e = tid;
-#pragma unroll 2
+#pragma unroll 4
                 for (int t = 0; t < C; t += 4) {
                     float4 w4;
                     float* wp = &w4.x;
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        wp[u] = (t + u < nc) ? bf16_to_f(vp[((size_t)(c0 + t + u) * H + h) * D + NE * r + e]) : 0.f;
+                        wp[u] = (t + u < nc)
+                            ? bf16_to_f(*reinterpret_cast<const uint16_t*>(sRawV + sw128_bf16(t + u, e))) : 0.f;
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, NE + D)) = w4;
                 }
             }
@@ -348,6 +452,14 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
             tc::mma_commit(mbar);
         }
         mma_wait();
+        // region RB is free again: fetch the next chunk's q, k, z into it
+        if (tid == 0 && has_next) {
+            tc::fence_proxy_async();
+            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
+            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, h * D, c0 + C, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, h * D, c0 + C, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, h * D, c0 + C, bar_in);
+        }
 
         // ---- 6. A1 = [-W ; Gamma Q - P Gamma K] in place of D[:, 64:192]
         {
@@ -433,17 +545,17 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
                     if (t < nc) {
                         const float tot = ss + s_rowsq[par * C + t];
                         const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                        const size_t rowoff = ((size_t)(c0 + t) * H + h) * D + NE * r;
-                        const uint16_t* gp = reinterpret_cast<const uint16_t*>(a.g_in) + rowoff;
-                        uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + rowoff;
+                        uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0 + t) * H + h) * D + NE * r;
 #pragma unroll
                         for (int c = 0; c < NE; c += 8) {
-                            float gv[8], yv[8];
-                            load8_bf16(gp + c, gv);
+                            const uint4 g8 = *reinterpret_cast<const uint4*>(sRawG + sw128_bf16(t, c));
+                            const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                            float yv[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
+                                const float gv = __uint_as_float((j & 1) ? (gw[j >> 1] & 0xffff0000u) : (gw[j >> 1] << 16));
                                 const float wn = a.norm_w ? a.norm_w[NE * r + c + j] : 1.f;
-                                yv[j] = sigmoidf_fast(gv[j]) * wn * o[c + j] * rr;
+                                yv[j] = sigmoidf_fast(gv) * wn * o[c + j] * rr;
                             }
                             store8_bf16(yp + c, yv);
                         }
@@ -452,6 +564,13 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
             }
         }
         __syncthreads();
+        // v and g_in of this chunk are consumed: fetch the next chunk's
+        if (tid == 0 && has_next) {
+            tc::fence_proxy_async();
+            tc::mbar_arrive_expect_tx(bar_vg, bytes_vg);
+            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, h * D + NE * r, c0 + C, bar_vg);
+            if (gate) tc::tma_load_2d(sm + OFF_RAWG, &tm_g, h * D + NE * r, c0 + C, bar_vg);
+        }
 
         // ---- 9. MMA 3: dS = (K gamma_C / Gamma)^T . V'
         if (tid == 0) {
@@ -510,6 +629,37 @@ prefill_tc_kernel(kda_prefill_args a, int* err) {
     if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// host: TMA descriptors
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D map over a [rows][row_elems] row-major tensor, box = box_cols x box_rows
+static cudaError_t make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr,
+                            uint64_t row_elems, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                            CUtensorMapSwizzle sw) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {row_elems, rows < 1 ? 1 : rows};
+    cuuint64_t strides[1] = {row_elems * esize};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace tcp
 
 bool prefill_tc_supported(const kda_prefill_args& a) {
@@ -520,16 +670,31 @@ bool prefill_tc_supported(const kda_prefill_args& a) {
 size_t prefill_tc_workspace_size(const kda_prefill_args&) { return 256; }
 
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tcp::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             tcp::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tcp::prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        tcp::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     if (a.num_seqs == 0) return cudaSuccess;
+    const uint64_t row = (uint64_t)a.H * tcp::D;
+    const uint64_t rows = (uint64_t)a.T_total;
+    CUtensorMap mq, mk, mz, mv, mg;
+    cudaError_t e;
+    if ((e = tcp::make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, row, rows, tcp::D, tcp::C,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = tcp::make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, row, rows, tcp::D, tcp::C,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = tcp::make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, row, rows, tcp::D, tcp::C,
+                           CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = tcp::make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, row, rows, tcp::NE, tcp::C,
+                           CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    if ((e = tcp::make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, row, rows, tcp::NE,
+                           tcp::C, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     dim3 grid(2, a.H, a.num_seqs);
-    tcp::prefill_tc_kernel<<<grid, tcp::NT, tcp::SMEM_BYTES, s>>>(a, reinterpret_cast<int*>(a.workspace));
+    tcp::prefill_tc_kernel<<<grid, tcp::NT, tcp::SMEM_BYTES, s>>>(a, reinterpret_cast<int*>(a.workspace),
+                                                                  mq, mk, mz, mv, mg);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -145,6 +145,27 @@ TC_DEV bool mbar_wait_bounded(uint64_t* mbar, uint32_t parity, uint32_t limit = 
     return false;
 }
 
+// expect `bytes` more transaction bytes on the mbarrier and arrive once
+TC_DEV void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA: 2-D tiled bulk copy global -> shared, completion counted on an mbarrier.
+// `map` is the address of a CUtensorMap kernel parameter (__grid_constant__);
+// (x, y) = (innermost, outer) element coordinates of the box origin.
+// ---------------------------------------------------------------------------
+TC_DEV void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
+}
+TC_DEV void tma_prefetch_desc(const void* map) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // FP32 -> TF32 (round to nearest, ties away), result kept in a 32-bit float
 // ---------------------------------------------------------------------------
