@@ -249,9 +249,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         // ---- 1b. gate, sub-chunk-relative decay factors, scaled q/k tiles (thread = channel d)
         {
             const int d = tid;
-            float tau[4];
             float pre = 1.f;                       // exp(G at the start of sub-chunk b)
-#pragma unroll
+#pragma unroll 1
             for (int b = 0; b < 4; ++b) {
                 float al[16], kv[16];
                 float F1 = 1.f;
@@ -276,12 +275,14 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                     sK[(16 * b + i) * QS + d] = kv[i] * F2;
                     F2 *= al[i];
                 }
-                tau[b] = F1;
                 s_tau[b * D + d] = F1;
                 s_expS[b * D + d] = pre;
                 pre *= F1;
             }
             s_gam[d] = pre;
+            float tau[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tau[b] = s_tau[b * D + d];
             float suf = 1.f;
 #pragma unroll
             for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= tau[b]; }
@@ -363,38 +364,129 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         __syncthreads();
 
-        // ---- 3. UT solve: rows of T = (I + A_kk)^{-1} (threads 0..63) and of
-        //         A_qk (I + A_kk)^{-1} (threads 64..127), then scale columns by beta.
-        //         Row i of either has zeros beyond column i, so a warp whose rows
-        //         are all below 32 skips the upper half of the sweep.
+        // ---- 3. UT solve, blockwise on 16x16 sub-blocks:
+        //         T = (I + A_kk)^{-1}:  T_aa = (I + A_aa)^{-1} (FP32 substitution),
+        //                               T_ab = -T_aa sum_{c=b}^{a-1} A_ac T_cb  (a > b)
+        //         P = A_qk T:           P_ab = sum_{c=b}^{a} Aqk_ac T_cb
+        //         The block products run as mma.sync tf32 in five dependency phases.
         {
-            const int i = tid & 63;
-            const bool isP = tid >= 64;
-            const int kmax = (warp & 1) ? C - 1 : 31;
-            float x[C];
+            float* sT = sAkk + C * AS;                 // T tile (region RB, after the Gram tiles)
+            float* sW = sT + C * AS;                   // per-warp 16x16 scratch for chained products
+            const int g = lane >> 2, t4 = lane & 3;
+            float* wsc = sW + warp * 16 * 16;
+            auto blk = [&](float* M, int a_, int b_) { return M + (16 * a_) * AS + 16 * b_; };
+            // acc += X(16x16, ld AS) * Y(16x16, ld ly)
+            auto mma16 = [&](float (&acc)[2][4], const float* X, const float* Y, int ly) {
 #pragma unroll
-            for (int j = 0; j < C; ++j) x[j] = isP ? (j <= i ? sAqk[i * AS + j] : 0.f) : (j == i ? 1.f : 0.f);
-            // x (I + A) = rhs, A strictly lower: x_j = rhs_j - sum_{k>j} x_k A[k][j]
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks + t4, k1 = k0 + 4;
+                    const float af[4] = {tc::to_tf32(X[g * AS + k0]), tc::to_tf32(X[(g + 8) * AS + k0]),
+                                         tc::to_tf32(X[g * AS + k1]), tc::to_tf32(X[(g + 8) * AS + k1])};
 #pragma unroll
-            for (int kk = C - 1; kk >= 1; --kk) {
-                if (kk <= kmax) {
-                    const float xk = x[kk];
-                    const float* row = sAkk + kk * AS;
-#pragma unroll
-                    for (int j4 = 0; j4 < kk; j4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(row + j4);
-                        x[j4] = fmaf(-xk, a4.x, x[j4]);
-                        if (j4 + 1 < kk) x[j4 + 1] = fmaf(-xk, a4.y, x[j4 + 1]);
-                        if (j4 + 2 < kk) x[j4 + 2] = fmaf(-xk, a4.z, x[j4 + 2]);
-                        if (j4 + 3 < kk) x[j4 + 3] = fmaf(-xk, a4.w, x[j4 + 3]);
+                    for (int nh = 0; nh < 2; ++nh) {
+                        const int nn = 8 * nh + g;
+                        const float bfr[2] = {tc::to_tf32(Y[k0 * ly + nn]), tc::to_tf32(Y[k1 * ly + nn])};
+                        tc::mma_m16n8k8_tf32(acc[nh], af, bfr);
                     }
                 }
-            }
-            float v[16];
+            };
+            auto zero = [&](float (&acc)[2][4]) {
 #pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) acc[nh][q4] = 0.f;
+            };
+            auto store = [&](const float (&acc)[2][4], float* Y, int ly, float sgn) {
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        Y[(g + (q4 >= 2 ? 8 : 0)) * ly + 8 * nh + 2 * t4 + (q4 & 1)] = sgn * acc[nh][q4];
+            };
+            // T_ab = -T_aa * (sum_{c=b}^{a-1} A_ac T_cb)
+            auto t_block = [&](int a_, int b_) {
+                float acc[2][4];
+                zero(acc);
+#pragma unroll 1
+                for (int c_ = b_; c_ < a_; ++c_) mma16(acc, blk(sAkk, a_, c_), blk(sT, c_, b_), AS);
+                store(acc, wsc, 16, 1.f);
+                __syncwarp();
+                float acc2[2][4];
+                zero(acc2);
+                mma16(acc2, blk(sT, a_, a_), wsc, 16);
+                store(acc2, blk(sT, a_, b_), AS, -1.f);
+                __syncwarp();
+            };
+            // P_ab = sum_{c=b}^{a} Aqk_ac T_cb, kept in registers until every read of Aqk is done
+            auto p_block = [&](float (&acc)[2][4], int a_, int b_) {
+                zero(acc);
+#pragma unroll 1
+                for (int c_ = b_; c_ <= a_; ++c_) mma16(acc, blk(sAqk, a_, c_), blk(sT, c_, b_), AS);
+            };
+
+            // phase A: diagonal inverses, thread (a, i) -> row i of (I + A_aa)^{-1}
+            if (tid < C) {
+                const int aa = tid >> 4, i = tid & 15;
+                const float* Ad = blk(sAkk, aa, aa);
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = (j == i) ? 1.f : 0.f;
+#pragma unroll
+                for (int kk = 15; kk >= 1; --kk) {
+                    const float xk = x[kk];
+#pragma unroll
+                    for (int j = 0; j < kk; ++j) x[j] = fmaf(-xk, Ad[kk * AS + j], x[j]);
+                }
+                float* Td = blk(sT, aa, aa) + i * AS;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) Td[j] = x[j];
+            }
+            __syncthreads();
+            // P blocks owned by each warp (kept in registers until every read of A_qk is done):
+            //   warp 0: P30   warp 1: P20   warp 2: P10 P21 P31   warp 3: P00 P11 P22 P33 P32
+            float pA[2][4], pB[2][4], pC[2][4], pD[2][4], pE[2][4];
+            // phase B: T10 T21 T32 on warps 0-2; warp 3: the diagonal P blocks
+            if (warp < 3) t_block(warp + 1, warp);
+            else { p_block(pA, 0, 0); p_block(pB, 1, 1); p_block(pC, 2, 2); p_block(pD, 3, 3); }
+            __syncthreads();
+            // phase C: T20 T31 on warps 0-1; P10 P21 on warp 2; P32 on warp 3
+            if (warp < 2) t_block(warp + 2, warp);
+            else if (warp == 2) { p_block(pA, 1, 0); p_block(pB, 2, 1); }
+            else p_block(pE, 3, 2);
+            __syncthreads();
+            // phase D: T30 on warp 0; P20 on warp 1; P31 on warp 2
+            if (warp == 0) t_block(3, 0);
+            else if (warp == 1) p_block(pA, 2, 0);
+            else if (warp == 2) p_block(pC, 3, 1);
+            __syncthreads();
+            // phase E: P30 on warp 0
+            if (warp == 0) p_block(pA, 3, 0);
+            __syncthreads();   // every read of A_qk is done: overwrite it with P
+            if (warp == 0) store(pA, blk(sAqk, 3, 0), AS, 1.f);
+            else if (warp == 1) store(pA, blk(sAqk, 2, 0), AS, 1.f);
+            else if (warp == 2) {
+                store(pA, blk(sAqk, 1, 0), AS, 1.f);
+                store(pB, blk(sAqk, 2, 1), AS, 1.f);
+                store(pC, blk(sAqk, 3, 1), AS, 1.f);
+            } else {
+                store(pA, blk(sAqk, 0, 0), AS, 1.f);
+                store(pB, blk(sAqk, 1, 1), AS, 1.f);
+                store(pC, blk(sAqk, 2, 2), AS, 1.f);
+                store(pD, blk(sAqk, 3, 3), AS, 1.f);
+                store(pE, blk(sAqk, 3, 2), AS, 1.f);
+            }
+            __syncthreads();
+            // rows of [T ; P] scaled by beta on the columns -> TMEM operand A2
+            const int i = tid & 63;
+            const float* src = (tid < C ? sT : sAqk) + i * AS;
+            float v[16];
+#pragma unroll 1
             for (int c = 0; c < C; c += 16) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(x[c + j] * s_beta[c + j]);
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c + j;
+                    v[j] = (col <= i) ? tc::to_tf32(src[col] * s_beta[col]) : 0.f;
+                }
                 tc::tmem_st16(T0 + TM_A2 + lane_base + c, v);
             }
         }

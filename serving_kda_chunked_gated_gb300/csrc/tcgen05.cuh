@@ -169,10 +169,10 @@ TC_DEV void tma_prefetch_desc(const void* map) {
 // ---------------------------------------------------------------------------
 // FP32 -> TF32 (round to nearest, ties away), result kept in a 32-bit float
 // ---------------------------------------------------------------------------
+// (integer form: add half a tf32 ulp to the magnitude and clear the 13 low
+// mantissa bits -- two full-rate integer operations; finite inputs)
 TC_DEV float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 // ---------------------------------------------------------------------------
