@@ -15,10 +15,10 @@
 //   S_next = Diag(gamma_C) S + (K (.) gamma_C / Gamma)^T V'                 (MMA 3)
 // (O = (Gamma Q) S + A_qk V' rearranged so that one MMA yields V' and O.)
 //
-// Work decomposition: a cluster of two CTAs per (sequence, head); CTA r owns
-// value columns [64r, 64r+64).  Both CTAs compute the d_k-wide chunk terms;
-// the only exchange is the per-row sum of squares for the RMSNorm of the
-// fused output gate (over distributed shared memory).
+// Work decomposition: a cluster of two CTAs (8 warps each) per (sequence,
+// head); CTA r owns value columns [64r, 64r+64).  Both CTAs compute the
+// d_k-wide chunk terms; the only exchange is the per-row sum of squares for
+// the RMSNorm of the fused output gate (over distributed shared memory).
 //
 // Data movement: each chunk's q, k, z tiles (64 x 128) and this CTA's v and
 // g_in tiles (64 x 64) arrive by TMA bulk tensor copies into shared memory,
@@ -45,7 +45,7 @@ namespace tcp {
 constexpr int C = 64;     // chunk length
 constexpr int D = 128;    // dk = dv
 constexpr int NE = 64;    // value columns per CTA
-constexpr int NT = 128;   // threads per CTA
+constexpr int NT = 256;   // threads per CTA (8 warps; warps w and w+4 share TMEM lanes)
 constexpr int QS = 132;   // padded row stride (floats) of the scaled q/k tiles
 constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
 constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
@@ -73,12 +73,14 @@ constexpr int OFF_SMALL = OFF_RAWV + VG_BYTES;
 // small region (floats)
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_ROWSQ = SM_GAM + D,
-              SM_CTAB = SM_ROWSQ + 2 * C, SM_FLOATS = SM_CTAB + NPAIR * D;
+              SM_ROWPART = SM_ROWSQ + 2 * C, SM_CTAB = SM_ROWPART + 2 * C, SM_FLOATS = SM_CTAB + NPAIR * D;
 constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 /*mbarriers, tmem base*/ + 1024 /*align*/;
 static_assert(OFF_VOP % 1024 == 0 && OFF_BPRE % 1024 == 0, "SW128 operands need 1024-B alignment");
 static_assert(OFF_RAWV % 1024 == 0 && OFF_RAWG % 1024 == 0, "128-B swizzled TMA tiles need 1024-B alignment");
 static_assert(2 * C * AS * 4 <= RB_BYTES && (NE + D) * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES,
               "region RB holds the raw tiles, the Gram tiles and [V|GK]^T in turn");
+static_assert(3 * C * AS * 4 + (NT / 32) * 16 * 16 * 4 <= RB_BYTES,
+              "region RB holds A_qk, A_kk, T and the per-warp solve scratch");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;   // one chunk of q, k, z
@@ -137,6 +139,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     float* s_expCE = fs + SM_EXPCE;  // [4][D] exp(G_C - G at sub-chunk end)
     float* s_gam = fs + SM_GAM;      // [D]    exp(G_C)
     float* s_rowsq = fs + SM_ROWSQ;  // [2][C] peer's row sums of squares (by chunk parity)
+    float* s_rowpart = fs + SM_ROWPART;  // [2][C] this CTA's row sums of squares, per column half
     float* s_ctab = fs + SM_CTAB;    // [NPAIR][D] exp(G_start(a) - G_end(b)), b < a; 1/tau_a for b = a
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
     uint64_t* bar_in = mbar + 1;
@@ -148,6 +151,9 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     const int n = blockIdx.z;
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // TMEM access: warp w reaches lanes 32*(w%4)..+31; warps w and w+4 split the columns
+    const int quad = warp & 3, hf = warp >> 2;
+    const int row = quad * 32 + lane;  // TMEM lane == operand row owned by this thread
     const int t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
     const float eA = __expf(a.A[h]);
     const bool gate = a.g_in != nullptr;
@@ -178,7 +184,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t T0 = *tbase_ptr;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int c_lo = hf * (NE / 2);    // this thread's half of a 64-column TMEM region
     uint32_t ph_mma = 0, ph_in = 0, ph_vg = 0;
     bool timed_out = false;
     auto mma_wait = [&]() {
@@ -190,13 +197,13 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     float beta_next = 0.f;
     if (tid < C && t_begin + tid < t_end) beta_next = a.beta[(size_t)(t_begin + tid) * H + h];
 
-    // ---- initial state -> TMEM master copy and the tf32 operand copy
+    // ---- initial state -> TMEM master copy and the tf32 operand copy (row d, 32 columns)
     {
-        const int d = tid;
+        const int d = row;
         const size_t sb = (((size_t)n * H + h) * D + d) * D + NE * r;
         float v[16];
 #pragma unroll
-        for (int c = 0; c < NE; c += 16) {
+        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = a.S0 ? a.S0[sb + c + j] : 0.f;
             tc::tmem_st16(T0 + TM_S + lane_base + c, v);
@@ -222,10 +229,10 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         if (!tc::mbar_wait_bounded(bar_in, ph_in, 1u << 22)) timed_out = true;
         ph_in ^= 1u;
 
-        // ---- 1a. q/k L2 norms (warp w: tokens 16w..16w+15) from the staged tiles
+        // ---- 1a. q/k L2 norms (warp w: tokens 8w..8w+7) from the staged tiles
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-            const int t = warp * 16 + i;
+        for (int i = 0; i < 8; ++i) {
+            const int t = warp * 8 + i;
             float sq = 0.f, sk = 0.f;
             if (t < nc) {
                 const uint2 qa = *reinterpret_cast<const uint2*>(sRawQ + t * D + 4 * lane);
@@ -246,12 +253,13 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         __syncthreads();
 
-        // ---- 1b. gate, sub-chunk-relative decay factors, scaled q/k tiles (thread = channel d)
+        // ---- 1b. gate and sub-chunk-relative decay factors: thread (channel d, half hf)
+        //          handles sub-chunks 2hf and 2hf+1 (the decay products restart at each
+        //          sub-chunk, so the halves are independent)
         {
-            const int d = tid;
-            float pre = 1.f;                       // exp(G at the start of sub-chunk b)
+            const int d = tid & (D - 1);
 #pragma unroll 1
-            for (int b = 0; b < 4; ++b) {
+            for (int b = 2 * (tid >> 7); b < 2 * (tid >> 7) + 2; ++b) {
                 float al[16], kv[16];
                 float F1 = 1.f;
 #pragma unroll
@@ -276,13 +284,18 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                     F2 *= al[i];
                 }
                 s_tau[b * D + d] = F1;
-                s_expS[b * D + d] = pre;
-                pre *= F1;
             }
-            s_gam[d] = pre;
+        }
+        __syncthreads();   // the raw q/k/z tiles are dead from here on
+        if (tid < D) {     // per-channel constants of the chunk (thread = channel d)
+            const int d = tid;
             float tau[4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) tau[b] = s_tau[b * D + d];
+            float pre = 1.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) { s_expS[b * D + d] = pre; pre *= tau[b]; }
+            s_gam[d] = pre;
             float suf = 1.f;
 #pragma unroll
             for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= tau[b]; }
@@ -302,62 +315,66 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                 }
             }
         }
-        __syncthreads();   // the raw q/k/z tiles are dead from here on
+        __syncthreads();
 
-        // ---- 2. Gram sub-blocks with mma.sync (tf32).  Warp w owns the QK blocks of
-        //         row block w and the KK blocks of row block 3-w: five 16x16 blocks,
-        //         ten independent accumulator chains.
+        // ---- 2. Gram sub-blocks with mma.sync (tf32): 20 block items (QK and KK for
+        //         the 10 pairs a >= b), warp w owns items w, w+8, w+16.
         {
             const int g = lane >> 2, t4 = lane & 3;
-            const int a0 = warp, a1 = 3 - warp, n0 = warp + 1;
-            float acc[5][2][4];
+            const int n_it = warp < 4 ? 3 : 2;
+            float acc[3][2][4];
 #pragma unroll
-            for (int it = 0; it < 5; ++it)
+            for (int it = 0; it < 3; ++it)
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
-            const int rq = 16 * a0 + g, rk = 16 * a1 + g;
+            int ia[3], ib[3], ip[3];
+#pragma unroll
+            for (int it = 0; it < 3; ++it) {
+                const int item = warp + 8 * it;              // 0..23 (>= 20 unused)
+                const int pr = item % NPAIR;                  // pair index a(a+1)/2 + b
+                const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
+                ia[it] = aa;
+                ib[it] = pr - aa * (aa + 1) / 2;
+                ip[it] = item >= NPAIR ? 1 : 0;               // 0: Q rows (A_qk), 1: K rows (A_kk)
+            }
 #pragma unroll 2
             for (int ks = 0; ks < 16; ++ks) {
                 const int k0 = 8 * ks + t4, k1 = k0 + 4;
-                const float aq[4] = {tc::to_tf32(sQ[rq * QS + k0]), tc::to_tf32(sQ[(rq + 8) * QS + k0]),
-                                     tc::to_tf32(sQ[rq * QS + k1]), tc::to_tf32(sQ[(rq + 8) * QS + k1])};
-                const float ak[4] = {tc::to_tf32(sKr[rk * QS + k0]), tc::to_tf32(sKr[(rk + 8) * QS + k0]),
-                                     tc::to_tf32(sKr[rk * QS + k1]), tc::to_tf32(sKr[(rk + 8) * QS + k1])};
 #pragma unroll
-                for (int it = 0; it < 5; ++it) {
-                    const bool p1 = it >= n0;
-                    const int aa = p1 ? a1 : a0;
-                    const int bb = p1 ? it - n0 : it;
-                    const float* ct = s_ctab + (aa * (aa + 1) / 2 + bb) * D;
-                    const float c0f = ct[k0], c1f = ct[k1];
-                    const float af[4] = {p1 ? ak[0] : aq[0], p1 ? ak[1] : aq[1],
-                                         p1 ? ak[2] : aq[2], p1 ? ak[3] : aq[3]};
+                for (int it = 0; it < 3; ++it) {
+                    if (it < n_it) {
+                        const float* Arow = ip[it] ? sKr : sQ;
+                        const int ra = 16 * ia[it] + g;
+                        const float af[4] = {tc::to_tf32(Arow[ra * QS + k0]), tc::to_tf32(Arow[(ra + 8) * QS + k0]),
+                                             tc::to_tf32(Arow[ra * QS + k1]), tc::to_tf32(Arow[(ra + 8) * QS + k1])};
+                        const float* ct = s_ctab + (ia[it] * (ia[it] + 1) / 2 + ib[it]) * D;
+                        const float c0f = ct[k0], c1f = ct[k1];
 #pragma unroll
-                    for (int nh = 0; nh < 2; ++nh) {
-                        const int j = 16 * bb + 8 * nh + g;
-                        const float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
-                        tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
+                        for (int nh = 0; nh < 2; ++nh) {
+                            const int j = 16 * ib[it] + 8 * nh + g;
+                            const float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
+                            tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
+                        }
                     }
                 }
             }
 #pragma unroll
-            for (int it = 0; it < 5; ++it) {
-                const bool p1 = it >= n0;
-                const int aa = p1 ? a1 : a0;
-                const int bb = p1 ? it - n0 : it;
-                float* Out = p1 ? sAkk : sAqk;
+            for (int it = 0; it < 3; ++it) {
+                if (it < n_it) {
+                    float* Out = ip[it] ? sAkk : sAqk;
 #pragma unroll
-                for (int nh = 0; nh < 2; ++nh) {
+                    for (int nh = 0; nh < 2; ++nh) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int I = 16 * aa + g + (q4 >= 2 ? 8 : 0);
-                        const int J = 16 * bb + 8 * nh + 2 * t4 + (q4 & 1);
-                        float val = acc[it][nh][q4];
-                        if (!p1) { if (J > I) val = 0.f; }
-                        else { val = (J >= I) ? 0.f : val * s_beta[I]; }
-                        Out[I * AS + J] = val;
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int I = 16 * ia[it] + g + (q4 >= 2 ? 8 : 0);
+                            const int J = 16 * ib[it] + 8 * nh + 2 * t4 + (q4 & 1);
+                            float val = acc[it][nh][q4];
+                            if (!ip[it]) { if (J > I) val = 0.f; }
+                            else { val = (J >= I) ? 0.f : val * s_beta[I]; }
+                            Out[I * AS + J] = val;
+                        }
                     }
                 }
             }
@@ -442,46 +459,44 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                 for (int j = 0; j < 16; ++j) Td[j] = x[j];
             }
             __syncthreads();
-            // P blocks owned by each warp (kept in registers until every read of A_qk is done):
-            //   warp 0: P30   warp 1: P20   warp 2: P10 P21 P31   warp 3: P00 P11 P22 P33 P32
-            float pA[2][4], pB[2][4], pC[2][4], pD[2][4], pE[2][4];
-            // phase B: T10 T21 T32 on warps 0-2; warp 3: the diagonal P blocks
+            // P blocks held in registers until every read of A_qk is done:
+            //   warp 2: P21   warp 3: P00 P32   warp 4: P11 P20   warp 5: P22 P31
+            //   warp 6: P33 P30   warp 7: P10
+            float pA[2][4], pB[2][4];
+            // phase B: T10 T21 T32 (warps 0-2), P00 P11 P22 P33 (warps 3-6)
             if (warp < 3) t_block(warp + 1, warp);
-            else { p_block(pA, 0, 0); p_block(pB, 1, 1); p_block(pC, 2, 2); p_block(pD, 3, 3); }
+            else if (warp < 7) p_block(pA, warp - 3, warp - 3);
             __syncthreads();
-            // phase C: T20 T31 on warps 0-1; P10 P21 on warp 2; P32 on warp 3
+            // phase C: T20 T31 (warps 0-1), P21 (warp 2), P32 (warp 3), P10 (warp 7)
             if (warp < 2) t_block(warp + 2, warp);
-            else if (warp == 2) { p_block(pA, 1, 0); p_block(pB, 2, 1); }
-            else p_block(pE, 3, 2);
+            else if (warp == 2) p_block(pA, 2, 1);
+            else if (warp == 3) p_block(pB, 3, 2);
+            else if (warp == 7) p_block(pA, 1, 0);
             __syncthreads();
-            // phase D: T30 on warp 0; P20 on warp 1; P31 on warp 2
+            // phase D: T30 (warp 0), P20 (warp 4), P31 (warp 5)
             if (warp == 0) t_block(3, 0);
-            else if (warp == 1) p_block(pA, 2, 0);
-            else if (warp == 2) p_block(pC, 3, 1);
+            else if (warp == 4) p_block(pB, 2, 0);
+            else if (warp == 5) p_block(pB, 3, 1);
             __syncthreads();
-            // phase E: P30 on warp 0
-            if (warp == 0) p_block(pA, 3, 0);
+            // phase E: P30 (warp 6)
+            if (warp == 6) p_block(pB, 3, 0);
             __syncthreads();   // every read of A_qk is done: overwrite it with P
-            if (warp == 0) store(pA, blk(sAqk, 3, 0), AS, 1.f);
-            else if (warp == 1) store(pA, blk(sAqk, 2, 0), AS, 1.f);
-            else if (warp == 2) {
-                store(pA, blk(sAqk, 1, 0), AS, 1.f);
-                store(pB, blk(sAqk, 2, 1), AS, 1.f);
-                store(pC, blk(sAqk, 3, 1), AS, 1.f);
-            } else {
-                store(pA, blk(sAqk, 0, 0), AS, 1.f);
-                store(pB, blk(sAqk, 1, 1), AS, 1.f);
-                store(pC, blk(sAqk, 2, 2), AS, 1.f);
-                store(pD, blk(sAqk, 3, 3), AS, 1.f);
-                store(pE, blk(sAqk, 3, 2), AS, 1.f);
+            switch (warp) {
+                case 2: store(pA, blk(sAqk, 2, 1), AS, 1.f); break;
+                case 3: store(pA, blk(sAqk, 0, 0), AS, 1.f); store(pB, blk(sAqk, 3, 2), AS, 1.f); break;
+                case 4: store(pA, blk(sAqk, 1, 1), AS, 1.f); store(pB, blk(sAqk, 2, 0), AS, 1.f); break;
+                case 5: store(pA, blk(sAqk, 2, 2), AS, 1.f); store(pB, blk(sAqk, 3, 1), AS, 1.f); break;
+                case 6: store(pA, blk(sAqk, 3, 3), AS, 1.f); store(pB, blk(sAqk, 3, 0), AS, 1.f); break;
+                case 7: store(pA, blk(sAqk, 1, 0), AS, 1.f); break;
+                default: break;
             }
             __syncthreads();
-            // rows of [T ; P] scaled by beta on the columns -> TMEM operand A2
-            const int i = tid & 63;
-            const float* src = (tid < C ? sT : sAqk) + i * AS;
+            // rows of [T ; P] scaled by beta on the columns -> TMEM operand A2 (32 columns each)
+            const int i = row & 63;
+            const float* src = (row < C ? sT : sAqk) + i * AS;
             float v[16];
-#pragma unroll 1
-            for (int c = 0; c < C; c += 16) {
+#pragma unroll
+            for (int c = c_lo; c < c_lo + C / 2; c += 16) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = c + j;
@@ -496,7 +511,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
 
         // ---- 4. B_pre = [V_half | Gamma K]^T (smem) and A3 = (K gamma_C / Gamma)^T (TMEM)
         {
-            if (tid < NE) {
+            if (tid < NE) {                      // rows 0..63: this CTA's value columns
                 const int e = tid;
 #pragma unroll 4
                 for (int t = 0; t < C; t += 4) {
@@ -508,20 +523,22 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                             ? bf16_to_f(*reinterpret_cast<const uint16_t*>(sRawV + sw128_bf16(t + u, e))) : 0.f;
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, NE + D)) = w4;
                 }
-            }
-            const int d = tid;
-#pragma unroll 2
-            for (int t = 0; t < C; t += 4) {
-                float4 w4;
-                float* wp = &w4.x;
-                const float es = s_expS[(t >> 4) * D + d];
+            } else if (tid < NE + D) {           // rows 64..191: (Gamma K)^T
+                const int d = tid - NE;
+#pragma unroll 4
+                for (int t = 0; t < C; t += 4) {
+                    float4 w4;
+                    float* wp = &w4.x;
+                    const float es = s_expS[(t >> 4) * D + d];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(sKr[(t + u) * QS + d] * es);
-                *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(NE + d, t, NE + D)) = w4;
+                    for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(sKr[(t + u) * QS + d] * es);
+                    *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(NE + d, t, NE + D)) = w4;
+                }
             }
+            const int d = row;                   // A3: lane d, this thread's 32 token columns
             float v[16];
 #pragma unroll
-            for (int c = 0; c < C; c += 16) {
+            for (int c = c_lo; c < c_lo + C / 2; c += 16) {
                 const float ec = s_expCE[(c >> 4) * D + d];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(sK[(c + j) * QS + d] * ec);
@@ -554,11 +571,13 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
 
         // ---- 6. A1 = [-W ; Gamma Q - P Gamma K] in place of D[:, 64:192]
+        //         (row = lane, this thread's 64 of the 128 columns)
         {
             float v[16];
-            if (tid < C) {
+            const int cbeg = NE + hf * (D / 2);
+            if (row < C) {
 #pragma unroll 1
-                for (int c = NE; c < NE + D; c += 16) {
+                for (int c = cbeg; c < cbeg + D / 2; c += 16) {
                     tc::tmem_ld16(T0 + TM_D + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
@@ -566,10 +585,10 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                     tc::tmem_st16(T0 + TM_D + lane_base + c, v);
                 }
             } else {
-                const int t = tid - C;
+                const int t = row - C;
                 const float* es = s_expS + (t >> 4) * D;
 #pragma unroll 1
-                for (int c = NE; c < NE + D; c += 16) {
+                for (int c = cbeg; c < cbeg + D / 2; c += 16) {
                     tc::tmem_ld16(T0 + TM_D + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
@@ -597,15 +616,15 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         mma_wait();
 
-        // ---- 8. V' -> operand (smem), O -> o and the fused output gate
+        // ---- 8. V' -> operand (smem), O -> o and the fused output gate (32 columns per thread)
         {
             float v[16];
-            float o[NE];
+            float o[NE / 2];
             float ss = 0.f;
-            if (tid < C) {
-                const int t = tid;
+            if (row < C) {
+                const int t = row;
 #pragma unroll
-                for (int c = 0; c < NE; c += 16) {
+                for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
                     tc::tmem_ld16(T0 + TM_D + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
@@ -613,40 +632,45 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                         *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + j, t, C)) = tc::to_tf32(v[j]);
                 }
             } else {
-                const int t = tid - C;
+                const int t = row - C;
 #pragma unroll
-                for (int c = 0; c < NE; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + c, v);
+                for (int c = 0; c < NE / 2; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + c_lo + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) { o[c + j] = a.scale * v[j]; ss += o[c + j] * o[c + j]; }
                 }
                 if (t < nc) {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0 + t) * H + h) * D + NE * r;
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
 #pragma unroll
-                    for (int c = 0; c < NE; c += 8) store8_bf16(dst + c, o + c);
+                    for (int c = 0; c < NE / 2; c += 8) store8_bf16(dst + c, o + c);
                 }
-                if (gate) st_cluster_f32(cluster_map(s_rowsq + par * C + t, r ^ 1), ss);
+                if (gate) s_rowpart[hf * C + t] = ss;
             }
             tc::fence_proxy_async();
             tc::fence_before_sync();
             if (gate) {
+                __syncthreads();
+                if (row >= C && hf == 0) {
+                    const int t = row - C;
+                    st_cluster_f32(cluster_map(s_rowsq + par * C + t, r ^ 1), s_rowpart[t] + s_rowpart[C + t]);
+                }
                 cluster_sync_all();
-                if (tid >= C) {
-                    const int t = tid - C;
+                if (row >= C) {
+                    const int t = row - C;
                     if (t < nc) {
-                        const float tot = ss + s_rowsq[par * C + t];
+                        const float tot = s_rowpart[t] + s_rowpart[C + t] + s_rowsq[par * C + t];
                         const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                        uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0 + t) * H + h) * D + NE * r;
+                        uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
 #pragma unroll
-                        for (int c = 0; c < NE; c += 8) {
-                            const uint4 g8 = *reinterpret_cast<const uint4*>(sRawG + sw128_bf16(t, c));
+                        for (int c = 0; c < NE / 2; c += 8) {
+                            const uint4 g8 = *reinterpret_cast<const uint4*>(sRawG + sw128_bf16(t, c_lo + c));
                             const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
                             float yv[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const float gv = __uint_as_float((j & 1) ? (gw[j >> 1] & 0xffff0000u) : (gw[j >> 1] << 16));
-                                const float wn = a.norm_w ? a.norm_w[NE * r + c + j] : 1.f;
+                                const float wn = a.norm_w ? a.norm_w[NE * r + c_lo + c + j] : 1.f;
                                 yv[j] = sigmoidf_fast(gv) * wn * o[c + j] * rr;
                             }
                             store8_bf16(yp + c, yv);
@@ -678,11 +702,11 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
 
         // ---- 10. S = Diag(gamma_C) S + dS  (FP32 in TMEM), refresh the tf32 operand copy
         {
-            const int d = tid;
+            const int d = row;
             const float gm = s_gam[d];
             float dv[16], sv[16];
 #pragma unroll
-            for (int c = 0; c < NE; c += 16) {
+            for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
                 tc::tmem_ld16(T0 + TM_DS + lane_base + c, dv);
                 tc::tmem_ld16(T0 + TM_S + lane_base + c, sv);
                 tc::tmem_ld_wait();
@@ -702,11 +726,11 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
 
     // ---- final state
     if (a.S_T) {
-        const int d = tid;
+        const int d = row;
         float* dst = a.S_T + (((size_t)n * H + h) * D + d) * D + NE * r;
         float v[16];
 #pragma unroll
-        for (int c = 0; c < NE; c += 16) {
+        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
             tc::tmem_ld16(T0 + TM_S + lane_base + c, v);
             tc::tmem_ld_wait();
 #pragma unroll
