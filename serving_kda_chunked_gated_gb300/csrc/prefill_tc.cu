@@ -315,40 +315,44 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                 }
             }
         }
-        __syncthreads();
+        // cluster-wide: the peer writes its Gram blocks into region RB only after both
+        // CTAs have consumed their raw q/k/z tiles there
+        cluster_sync_all();
 
-        // ---- 2. Gram sub-blocks with mma.sync (tf32): 20 block items (QK and KK for
-        //         the 10 pairs a >= b), warp w owns items w, w+8, w+16.
+        // ---- 2. Gram sub-blocks with mma.sync (tf32), split over the cluster: CTA 0
+        //         forms A_qk, CTA 1 forms A_kk (10 blocks of 16x16 each; warp w owns pairs
+        //         w and w+8) and writes every block to its own and to its peer's tile.
         {
             const int g = lane >> 2, t4 = lane & 3;
-            const int n_it = warp < 4 ? 3 : 2;
-            float acc[3][2][4];
+            const bool kk_pass = r == 1;
+            const float* Arows = kk_pass ? sKr : sQ;
+            float* Out = kk_pass ? sAkk : sAqk;
+            const uint32_t out_peer = cluster_map(Out, r ^ 1);
+            const int n_it = warp < NPAIR - 8 ? 2 : 1;
+            float acc[2][2][4];
 #pragma unroll
-            for (int it = 0; it < 3; ++it)
+            for (int it = 0; it < 2; ++it)
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
-            int ia[3], ib[3], ip[3];
+            int ia[2], ib[2];
 #pragma unroll
-            for (int it = 0; it < 3; ++it) {
-                const int item = warp + 8 * it;              // 0..23 (>= 20 unused)
-                const int pr = item % NPAIR;                  // pair index a(a+1)/2 + b
+            for (int it = 0; it < 2; ++it) {
+                const int pr = warp + 8 * it;                 // pair index a(a+1)/2 + b
                 const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
                 ia[it] = aa;
                 ib[it] = pr - aa * (aa + 1) / 2;
-                ip[it] = item >= NPAIR ? 1 : 0;               // 0: Q rows (A_qk), 1: K rows (A_kk)
             }
 #pragma unroll 2
             for (int ks = 0; ks < 16; ++ks) {
                 const int k0 = 8 * ks + t4, k1 = k0 + 4;
 #pragma unroll
-                for (int it = 0; it < 3; ++it) {
+                for (int it = 0; it < 2; ++it) {
                     if (it < n_it) {
-                        const float* Arow = ip[it] ? sKr : sQ;
                         const int ra = 16 * ia[it] + g;
-                        const float af[4] = {tc::to_tf32(Arow[ra * QS + k0]), tc::to_tf32(Arow[(ra + 8) * QS + k0]),
-                                             tc::to_tf32(Arow[ra * QS + k1]), tc::to_tf32(Arow[(ra + 8) * QS + k1])};
+                        const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
+                                             tc::to_tf32(Arows[ra * QS + k1]), tc::to_tf32(Arows[(ra + 8) * QS + k1])};
                         const float* ct = s_ctab + (ia[it] * (ia[it] + 1) / 2 + ib[it]) * D;
                         const float c0f = ct[k0], c1f = ct[k1];
 #pragma unroll
@@ -361,25 +365,31 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                 }
             }
 #pragma unroll
-            for (int it = 0; it < 3; ++it) {
+            for (int it = 0; it < 2; ++it) {
                 if (it < n_it) {
-                    float* Out = ip[it] ? sAkk : sAqk;
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int I = 16 * ia[it] + g + (q4 >= 2 ? 8 : 0);
-                            const int J = 16 * ib[it] + 8 * nh + 2 * t4 + (q4 & 1);
-                            float val = acc[it][nh][q4];
-                            if (!ip[it]) { if (J > I) val = 0.f; }
-                            else { val = (J >= I) ? 0.f : val * s_beta[I]; }
-                            Out[I * AS + J] = val;
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int I = 16 * ia[it] + g + 8 * hr;
+                            const int J = 16 * ib[it] + 8 * nh + 2 * t4;
+                            float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
+                            if (!kk_pass) { if (J > I) v0 = 0.f; if (J + 1 > I) v1 = 0.f; }
+                            else {
+                                const float bI = s_beta[I];
+                                v0 = (J >= I) ? 0.f : v0 * bI;
+                                v1 = (J + 1 >= I) ? 0.f : v1 * bI;
+                            }
+                            const int off = I * AS + J;
+                            *reinterpret_cast<float2*>(Out + off) = make_float2(v0, v1);
+                            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};"
+                                         :: "r"(out_peer + 4u * (uint32_t)off), "f"(v0), "f"(v1) : "memory");
                         }
                     }
                 }
             }
         }
-        __syncthreads();
+        cluster_sync_all();   // both halves of the Gram are in both CTAs
 
         // ---- 3. UT solve, blockwise on 16x16 sub-blocks:
         //         T = (I + A_kk)^{-1}:  T_aa = (I + A_aa)^{-1} (FP32 substitution),
