@@ -163,6 +163,18 @@ def make_decode_inputs(torch, dev, seed, N=256, H=32, d=128):
     }
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over the process group (identity without one).
+    The step time of the job is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
@@ -238,11 +250,7 @@ def run_ours(args, rank, world):
     barrier()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_all = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_all = float(t.item())
+    ms_all = max_over_ranks(ms, dev)
 
     # ---- decode step (secondary): state read + written once per step
     dec = make_decode_inputs(torch, dev, seed=99 + rank)

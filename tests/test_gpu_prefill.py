@@ -151,3 +151,66 @@ def test_full_varlen_16_sampled(kda_lib, cuda_dev):
         sub["cu_seqlens"] = np.array([0, e - s], dtype=np.int32)
         o1, S1, _ = run_gpu(kda, sub, cuda_dev)
         assert torch.equal(o1, o[s:e]) and torch.equal(S1[0], S_T[n])
+
+
+def test_prefill_then_decode_continues_the_sequence(kda_lib, cuda_dev):
+    """Prefill 150 tokens on the tensor-core path, then decode 3 more with
+    kda_decode_step from its final state: every output matches the oracle's
+    single 153-token recurrence (the prefix cache resumes exactly)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=153, H=2))
+    T0 = 150
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
+    g_in = to_dev(d["g_in"], cuda_dev, True)
+    S0 = to_dev(d["S0"], cuda_dev)
+    o, S, y = kda.prefill(q[:T0].contiguous(), k[:T0].contiguous(), v[:T0].contiguous(), z[:T0].contiguous(),
+                          beta[:T0].contiguous(), A, S0=S0, g_in=g_in[:T0].contiguous())
+    outs, ys = [o], [y]
+    for t in range(T0, 153):
+        sl = slice(t, t + 1)
+        # fresh copies: a one-token slice of a packed tensor is not 16-byte aligned
+        od, yd = kda.decode_step(q[sl].clone(), k[sl].clone(), v[sl].clone(), z[sl].clone(),
+                                 beta[sl].clone(), A, S, g_in=g_in[sl].clone())
+        outs.append(od)
+        ys.append(yd)
+    torch.cuda.synchronize()
+    ro, rS, ry = run_oracle(d)
+    assert rel(host(torch.cat(outs)), ro) < TOL_O
+    assert rel(host(torch.cat(ys)), ry) < TOL_O
+    assert rel(host(S), rS) < TOL_S
+
+
+def test_split_prefill_resumes_from_state(kda_lib, cuda_dev):
+    """prefill(T1) then prefill(T2 | S_T1) equals the oracle on T1 + T2 tokens."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=333, H=2))
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
+    S0 = to_dev(d["S0"], cuda_dev)
+    c = lambda x, s: x[s].clone()
+    a, b = slice(0, 100), slice(100, 333)
+    o1, S1, _ = kda.prefill(c(q, a), c(k, a), c(v, a), c(z, a), c(beta, a), A, S0=S0)
+    o2, S2, _ = kda.prefill(c(q, b), c(k, b), c(v, b), c(z, b), c(beta, b), A, S0=S1)
+    torch.cuda.synchronize()
+    ro, rS, _ = run_oracle(d, gate=False)
+    assert rel(host(torch.cat([o1, o2])), ro) < TOL_O
+    assert rel(host(S2), rS) < TOL_S
+
+
+def test_options_scale_norm_weight_no_l2norm(kda_lib, cuda_dev):
+    """scale != 1, an RMSNorm weight, and qk_l2norm off (inputs pre-normalised)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=130, H=2))
+    w = (np.random.default_rng(5).random(128) + 0.5).astype(np.float32)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    o, S_T, y = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev),
+                            to_dev(d["A"], cuda_dev), S0=to_dev(d["S0"], cuda_dev),
+                            g_in=to_dev(d["g_in"], cuda_dev, True), norm_w=to_dev(w, cuda_dev),
+                            scale=0.5, qk_l2norm=False)
+    torch.cuda.synchronize()
+    ro, rS, ry = oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"],
+                                S0=d["S0"], g_in=f64(d, "g_in"), norm_w=w, scale=0.5, qk_l2norm=False)
+    assert rel(host(o), ro) < TOL_O
+    assert rel(host(y), ry) < TOL_O
+    assert rel(host(S_T), rS) < TOL_S
