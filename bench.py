@@ -34,6 +34,7 @@ METRIC = "KDA prefill tokens/s (% BF16 TC peak); decode-step HBM GB/s (% of peak
 # algorithmic work per token per head (d = 128, chunk 64): 6 d^2 + 5 d (C+1) + C^2/3 flop
 FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 128 * 65 + 64 * 64 // 3
 TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 : bf16 ratio (GB300)
+SNAP_INTERVAL = 1024            # prefix-cache block: one state snapshot per 1024 tokens
 
 WORKLOADS = {
     "prefill_128k": dict(T=131072, H=32, d=128, S0=True, gate=True, varlen=None),
@@ -270,6 +271,24 @@ def run_ours(args, rank, world):
     d1.record(stream)
     torch.cuda.synchronize()
     dec_ms = d0.elapsed_time(d1) / dsteps
+
+    # ---- prefix-cache snapshots (secondary): the same prefill writing the state
+    # every SNAP_INTERVAL tokens of each sequence
+    snap_rows = kda.snapshot_count(cu_host.tolist(), SNAP_INTERVAL)
+    S_snap = torch.empty((max(snap_rows, 1), H, d, d), dtype=torch.float32, device=dev)
+    ps = kda.PrefillArgs.from_buffer_copy(pa)
+    ps.snap_interval, ps.S_snap = SNAP_INTERVAL, S_snap.data_ptr()
+    for _ in range(max(args.warmup, 3)):
+        kda.prefill_raw(ps, stream)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        kda.prefill_raw(ps, stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    snap_ms = p0.elapsed_time(p1) / args.steps
+    del S_snap
     clocks = sampler.stop()
 
     # ---- end to end: host buffers in, host buffers out, through the public call
@@ -353,6 +372,10 @@ def run_ours(args, rank, world):
                                 "frac": dec_gbs / pk["hbm"],
                                 "traffic": kernel_traffic("decode.cu", "decode"),
                                 "algorithmic_bytes_per_launch": dec_bytes}},
+        "prefix_cache": {"snap_interval": SNAP_INTERVAL, "snapshots_per_launch": snap_rows * H,
+                         "snapshot_bytes_per_launch": snap_rows * H * d * d * 4,
+                         "ms_per_step": snap_ms, "overhead_vs_plain": snap_ms / ms - 1.0,
+                         "value": world * T / (snap_ms * 1e-3), "unit": "tokens/s"},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,

@@ -53,7 +53,12 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 
 /*
  * Chunked prefill over packed sequences (Sec. 2.1 chunked form, Sec. 2.2
- * 16-token sub-chunks; chunk length 64).
+ * 16-token sub-chunks; chunk length 64), with optional prefix-cache state
+ * snapshots at chunk-aligned intervals (Sec. 13.1: a cached prefix is only
+ * reusable where the recurrent state can be restored at the same boundary;
+ * "Kimi-K3 深度技术分析" (liuhc.cn), Sec. 5.2 KDA Prefill Cache: the state is
+ * cached per contiguous block, and a new request resumes its prefill from the
+ * nearest cached block boundary).
  *
  * Token layout: the T_total tokens of num_seqs sequences are packed; sequence n
  * owns tokens [cu_seqlens[n], cu_seqlens[n+1]).  cu_seqlens is a DEVICE int32
@@ -105,9 +110,26 @@ typedef struct {
     void* y;
     void* workspace;
     size_t workspace_bytes;
+    /* Prefix-cache snapshots (optional): when S_snap is non-NULL, the FP32
+     * state of sequence n after every snap_interval of its tokens is written to
+     * S_snap [rows, H, dk, dv]: the state after token j*snap_interval (counted
+     * from the sequence start), j = 1 .. floor(len_n / snap_interval), goes to
+     * row snap_base(n) + j - 1, where snap_base(n) sums floor(len_m /
+     * snap_interval) over the sequences m < n.  snap_interval must be a
+     * positive multiple of 64 (the chunk length), so snapshots sit on chunk
+     * boundaries and a later prefill can resume from any of them through S0.
+     * kda_prefill_snapshot_count() gives the number of rows.  Errors: another
+     * snap_interval -> KDA_ERR_SHAPE; S_snap not 16-byte aligned ->
+     * KDA_ERR_ALIGN.  S_snap must not overlap any other argument.  Ignored
+     * (and snap_interval unread) when S_snap is NULL. */
+    int snap_interval;
+    float* S_snap;
 } kda_prefill_args;
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* args);
+/* Rows S_snap must hold for these arguments (0 when snapshots are off or the
+ * arguments are invalid); computed on the host from cu_seqlens_host. */
+long kda_prefill_snapshot_count(const kda_prefill_args* args);
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 
 /*

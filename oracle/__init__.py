@@ -64,7 +64,7 @@ def _load():
         lib.kda_oracle_prefill.argtypes = [
             ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int, ctypes.c_int,
             d, d, d, d, d, d, ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_double,
-            d, d, d, d, d, ctypes.c_double, d]
+            d, d, d, d, d, ctypes.c_double, d, ctypes.c_int, d]
         lib.kda_oracle_log_decay.restype = ctypes.c_double
         lib.kda_oracle_log_decay.argtypes = [ctypes.c_double] * 3
         lib.kda_oracle_gate_norm.restype = None
@@ -103,12 +103,15 @@ def log_decay(z, A_h: float, g_min: float = G_MIN) -> np.ndarray:
 
 def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
             g_min=G_MIN, scale=1.0, qk_l2norm=True, l2_eps=L2_EPS, norm_eps=NORM_EPS,
-            want_state=True):
+            want_state=True, snap_interval=0):
     """Per-token recurrence, Sec. 2.1, over packed sequences.
 
     q, k, z: [tok, H, dk]; v: [tok, H, dv]; beta: [tok, H]; A: [H];
     cu_seqlens: int32 [N+1] (None = one sequence); S0: [N, H, dk, dv] or None.
-    Returns (o [tok,H,dv], S_T [N,H,dk,dv] or None, y [tok,H,dv] or None), FP64.
+    Returns (o [tok,H,dv], S_T [N,H,dk,dv] or None, y [tok,H,dv] or None), FP64,
+    and, when snap_interval > 0, the prefix-cache snapshots [rows, H, dk, dv]:
+    the state of each sequence after every snap_interval of its tokens, the
+    sequences' rows in order (Sec. 13.1 prefix cache).
     """
     lib = _load()
     q, k, v, z, beta, A = map(_f64, (q, k, v, z, beta, A))
@@ -124,11 +127,18 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
     o = np.zeros((tok, H, dv))
     S_T = np.zeros((N, H, dk, dv)) if want_state else None
     y = np.zeros((tok, H, dv)) if g_in is not None else None
+    S_snap = None
+    if snap_interval:
+        rows = int(sum((int(cu[i + 1]) - int(cu[i])) // snap_interval for i in range(N)))
+        S_snap = np.zeros((rows, H, dk, dv))
     lib.kda_oracle_prefill(
         N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), H, dk, dv,
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
         float(g_min), float(scale), int(bool(qk_l2norm)), float(l2_eps),
-        _ptr(S0), _ptr(o), _ptr(S_T), _ptr(g_in), _ptr(norm_w), float(norm_eps), _ptr(y))
+        _ptr(S0), _ptr(o), _ptr(S_T), _ptr(g_in), _ptr(norm_w), float(norm_eps), _ptr(y),
+        int(snap_interval), _ptr(S_snap) if S_snap is not None and S_snap.size else None)
+    if snap_interval:
+        return o, S_T, y, S_snap
     return o, S_T, y
 
 

@@ -18,6 +18,12 @@
  *   product are outside this operator; g_in = W_g x is an input):
  *       y_t = Sigmoid(g_in_t) (.) RMSNorm(o~_t).
  *
+ * Sec. 13.1, prefix cache: a cached prefix is reusable only where the
+ * recurrent state can be restored at the same boundary.  With snap_interval > 0
+ * the state of each sequence after every snap_interval of its tokens is copied
+ * out (S_snap, rows of all sequences in order), so a later prefill can resume
+ * from any of those boundaries through S0.
+ *
  * The update is evaluated in the algebraically identical delta form
  *       S <- Diag(alpha) S;  u = beta (v - S^T k);  S <- S + k u^T
  * since (I - beta k k^T) X + beta k v^T = X + k (beta (v - X^T k))^T for
@@ -78,7 +84,7 @@ void kda_oracle_prefill(int num_seqs, const int32_t* cu_seqlens, int H, int dk, 
                         double g_min, double scale, int qk_l2norm, double l2_eps,
                         const double* S0, double* o, double* S_T,
                         const double* g_in, const double* norm_w, double norm_eps,
-                        double* y) {
+                        double* y, int snap_interval, double* S_snap) {
     long pairs = (long)num_seqs * H;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)
@@ -94,6 +100,10 @@ void kda_oracle_prefill(int num_seqs, const int32_t* cu_seqlens, int H, int dk, 
         if (S0) memcpy(S, S0 + sbase, sizeof(double) * (size_t)dk * dv);
         else memset(S, 0, sizeof(double) * (size_t)dk * dv);
         double eA = exp(A[h]);
+        /* prefix-cache snapshots: rows of the sequences before this one come first */
+        long snap_row = 0;
+        if (S_snap)
+            for (int m = 0; m < n; ++m) snap_row += (cu_seqlens[m + 1] - cu_seqlens[m]) / snap_interval;
         for (long t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
             const double* qt = q + ((size_t)t * H + h) * dk;
             const double* kt = k + ((size_t)t * H + h) * dk;
@@ -124,6 +134,12 @@ void kda_oracle_prefill(int num_seqs, const int32_t* cu_seqlens, int H, int dk, 
             if (g_in && y)
                 kda_oracle_gate_norm_row(out, g_in + ((size_t)t * H + h) * dv, norm_w, norm_eps,
                                          y + ((size_t)t * H + h) * dv, dv);
+            /* S is now the state after token t; keep it when t closes an interval */
+            if (S_snap && (t + 1 - cu_seqlens[n]) % snap_interval == 0) {
+                memcpy(S_snap + ((size_t)snap_row * H + h) * (size_t)dk * dv, S,
+                       sizeof(double) * (size_t)dk * dv);
+                ++snap_row;
+            }
         }
         if (S_T) memcpy(S_T + sbase, S, sizeof(double) * (size_t)dk * dv);
         free(S); free(qn); free(kn); free(u); free(ot);

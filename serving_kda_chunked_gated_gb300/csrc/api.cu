@@ -80,8 +80,19 @@ static kda_status validate_prefill(const kda_prefill_args* a) {
     for (int n = 0; n < a->num_seqs; ++n)
         if (cu[n + 1] < cu[n]) return KDA_ERR_SEQLENS;
     if (cu[a->num_seqs] != a->T_total) return KDA_ERR_SEQLENS;
-    // S0 may alias S_T exactly; any other overlap between outputs and inputs is rejected.
+    if (a->S_snap) {
+        if (a->snap_interval <= 0 || a->snap_interval % 64 != 0) return KDA_ERR_SHAPE;
+        if (misaligned(a->S_snap)) return KDA_ERR_ALIGN;
+    }
     return KDA_OK;
+}
+
+long kda_prefill_snapshot_count(const kda_prefill_args* a) {
+    if (validate_prefill(a) != KDA_OK || !a->S_snap) return 0;
+    long rows = 0;
+    for (int n = 0; n < a->num_seqs; ++n)
+        rows += (a->cu_seqlens_host[n + 1] - a->cu_seqlens_host[n]) / a->snap_interval;
+    return rows;
 }
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* a) {

@@ -28,6 +28,16 @@ KDA_DEV uint16_t f_to_bf16(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// First prefix-cache snapshot row of sequence n: the whole snapshot intervals in
+// the sequences before it.  Called by every lane of a warp; all get the value.
+KDA_DEV long snapshot_row_base(const int* cu_seqlens, int n, int interval) {
+    long s = 0;
+    for (int m = threadIdx.x & 31; m < n; m += 32) s += (cu_seqlens[m + 1] - cu_seqlens[m]) / interval;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
+}
+
 KDA_DEV float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

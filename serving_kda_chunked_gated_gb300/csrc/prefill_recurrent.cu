@@ -37,6 +37,9 @@ prefill_recurrent_kernel(kda_prefill_args a) {
         else st[r] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const float eA = __expf(a.A[h]);
+    // prefix-cache snapshots: the next row to write and the tokens until it is due
+    long snap_row = a.S_snap ? snapshot_row_base(a.cu_seqlens, n, a.snap_interval) : 0;
+    int snap_left = a.snap_interval;
 
     for (int t = t0; t < t1; ++t) {
         const size_t tok = (size_t)t * a.H + h;
@@ -108,6 +111,14 @@ prefill_recurrent_kernel(kda_prefill_args a) {
             const float gi = bf16_to_f(reinterpret_cast<const uint16_t*>(a.g_in)[tok * D + tid]);
             const float wn = a.norm_w ? a.norm_w[tid] : 1.0f;
             reinterpret_cast<uint16_t*>(a.y)[tok * D + tid] = f_to_bf16(sigmoidf_fast(gi) * wn * o_e * r);
+        }
+        if (a.S_snap && --snap_left == 0) {
+            float* dst = a.S_snap + ((size_t)snap_row * a.H + h) * (size_t)D * D;
+#pragma unroll
+            for (int r = 0; r < RPG; ++r)
+                *reinterpret_cast<float4*>(dst + (size_t)(rg * RPG + r) * D + 4 * cg) = st[r];
+            ++snap_row;
+            snap_left = a.snap_interval;
         }
         __syncthreads();   // shared buffers are rewritten by the next token
     }

@@ -710,10 +710,17 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         mma_wait();
 
-        // ---- 10. S = Diag(gamma_C) S + dS  (FP32 in TMEM), refresh the tf32 operand copy
+        // ---- 10. S = Diag(gamma_C) S + dS  (FP32 in TMEM), refresh the tf32 operand copy;
+        //          a chunk that closes a prefix-cache interval also writes S out
         {
             const int d = row;
             const float gm = s_gam[d];
+            float* snap = nullptr;
+            if (a.S_snap && (c0 + nc - t_begin) % a.snap_interval == 0) {
+                const long srow = snapshot_row_base(a.cu_seqlens, n, a.snap_interval) +
+                                  (c0 + nc - t_begin) / a.snap_interval - 1;
+                snap = a.S_snap + ((srow * H + h) * D + d) * D + NE * r;
+            }
             float dv[16], sv[16];
 #pragma unroll
             for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
@@ -723,6 +730,11 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
 #pragma unroll
                 for (int j = 0; j < 16; ++j) sv[j] = fmaf(gm, sv[j], dv[j]);
                 tc::tmem_st16(T0 + TM_S + lane_base + c, sv);
+                if (snap) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4*>(snap + c + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + j, d, NE)) = tc::to_tf32(sv[j]);

@@ -23,7 +23,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
-            "kda_version", "kda_launch_count", "kda_prefill_noalloc"]
+            "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count"]
 
 _vp = ctypes.c_void_p
 
@@ -39,6 +39,7 @@ class PrefillArgs(ctypes.Structure):
         ("S0", _vp), ("o", _vp), ("S_T", _vp),
         ("g_in", _vp), ("norm_w", _vp), ("norm_eps", ctypes.c_float), ("y", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("snap_interval", ctypes.c_int), ("S_snap", _vp),
     ]
 
 
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_prefill_recurrent.restype = ctypes.c_int
     lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_prefill_snapshot_count.argtypes = [ctypes.POINTER(PrefillArgs)]
+    lib.kda_prefill_snapshot_count.restype = ctypes.c_long
     lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_gate_norm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, ctypes.c_long,
@@ -166,13 +169,20 @@ def prefill_raw(args: PrefillArgs, stream=None, recurrent: bool = False):
     _check(fn(ctypes.byref(args), _stream(stream)), "kda_prefill_recurrent" if recurrent else "kda_prefill")
 
 
+def snapshot_count(cu_seqlens_host, interval: int) -> int:
+    """Rows of the snapshot output for packed sequences (see kda.h)."""
+    cu = [int(x) for x in cu_seqlens_host]
+    return sum((cu[i + 1] - cu[i]) // interval for i in range(len(cu) - 1))
+
+
 def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
             g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, want_state=True,
-            out=None, stream=None, recurrent=False, workspace=None):
+            out=None, stream=None, recurrent=False, workspace=None, snap_interval=0):
     """KDA chunked prefill through ``kda_prefill``.
 
     q, k, z: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; A: [H]; cu_seqlens: int32
-    [N+1] on the device (None = one sequence).  Returns (o, S_T, y).
+    [N+1] on the device (None = one sequence).  Returns (o, S_T, y), or
+    (o, S_T, y, S_snap) when snap_interval > 0 (prefix-cache snapshots).
     """
     T, H, dk = q.shape
     dv = v.shape[2]
@@ -190,6 +200,13 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
     args = make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_host, o, S0=S0, S_T=S_T,
                              g_in=g_in, norm_w=norm_w, y=y, g_min=g_min, scale=scale,
                              qk_l2norm=qk_l2norm, norm_eps=norm_eps)
+    S_snap = None
+    if snap_interval:
+        rows = snapshot_count(cu_host.tolist(), snap_interval)
+        S_snap = torch.empty((max(rows, 1), H, dk, dv), dtype=torch.float32, device=dev)
+        args.snap_interval = int(snap_interval)
+        args.S_snap = S_snap.data_ptr()
+        S_snap = S_snap[:rows]
     if not recurrent:
         need = prefill_workspace_size(args)
         if need > 0:
@@ -198,6 +215,8 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
             args.workspace = workspace.data_ptr()
             args.workspace_bytes = workspace.numel() * workspace.element_size()
     prefill_raw(args, stream=stream, recurrent=recurrent)
+    if snap_interval:
+        return o, S_T, y, S_snap
     return o, S_T, y
 
 

@@ -71,6 +71,8 @@ def _args(kda, **kw):
     (dict(dk=96, dv=96), 2), (dict(dk=128, dv=64), 2), (dict(H=0), 2),
     (dict(qkv_dtype=5), 3), (dict(q=FAKE + 4), 4), (dict(o=FAKE + 8), 4),
     (dict(T_total=65), 5), (dict(g_in=FAKE), 1),
+    (dict(S_snap=FAKE, snap_interval=0), 2), (dict(S_snap=FAKE, snap_interval=96), 2),
+    (dict(S_snap=FAKE + 4, snap_interval=64), 4),
 ])
 def test_prefill_validation(kda_lib, mutate, expect):
     import serving_kda_chunked_gated_gb300.kda as kda
@@ -92,6 +94,22 @@ def test_prefill_seqlens_validation(kda_lib):
     a2, _c = _args(kda, g_in=FAKE, y=FAKE, qkv_dtype=kda.KDA_F32)
     assert kda_lib.kda_prefill(ctypes.byref(a2), None) == 3
     assert kda_lib.kda_prefill_workspace_size(ctypes.byref(a2)) == 0
+
+
+def test_snapshot_count(kda_lib):
+    """Rows of the prefix-cache snapshot output: whole intervals per sequence."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    cu = np.array([0, 0, 130, 150, 343, 407], dtype=np.int32)
+    a, _ = _args(kda, num_seqs=5, T_total=407, cu_seqlens_host=cu.ctypes.data,
+                 S_snap=FAKE, snap_interval=64)
+    assert kda_lib.kda_prefill_snapshot_count(ctypes.byref(a)) == 2 + 0 + 3 + 1
+    a.snap_interval = 128
+    assert kda_lib.kda_prefill_snapshot_count(ctypes.byref(a)) == 1 + 0 + 1 + 0
+    assert kda.snapshot_count(cu, 128) == 2 and kda.snapshot_count(cu, 64) == 6
+    a.snap_interval = 100                                   # not a multiple of the chunk
+    assert kda_lib.kda_prefill_snapshot_count(ctypes.byref(a)) == 0
+    a.snap_interval, a.S_snap = 64, None                    # snapshots off
+    assert kda_lib.kda_prefill_snapshot_count(ctypes.byref(a)) == 0
 
 
 def test_decode_and_gate_norm_validation(kda_lib):

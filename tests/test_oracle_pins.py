@@ -2,7 +2,8 @@
 
 Page: "Kimi K3: KDA, attention residuals and Stable LatentMoE" (hs-black.github.io),
 Sec. 2.1 (recurrence, chunked form), Sec. 2.2 (bounded gate, 16-token
-sub-chunks, e^80 bound), Sec. 2.3 (output gate), Sec. 10.2 (KCP pairs).
+sub-chunks, e^80 bound), Sec. 2.3 (output gate), Sec. 10.2 (KCP pairs),
+Sec. 13.1 (prefix cache: states restorable at block boundaries).
 
 Each pin is chosen so that a plausible slip in the oracle (a dropped decay, a
 sign, a transposed readout, a wrong index) fails at least one of them; the
@@ -303,6 +304,37 @@ def test_l2norm_flag():
 
 
 # --------------------------------------------------------------------------
+# 13. Prefix-cache snapshots (Sec. 13.1): the state after every interval of a
+#     sequence is the final state of a prefill of that prefix alone, and a
+#     prefill resumed from it reproduces the rest of the sequence
+# --------------------------------------------------------------------------
+
+def test_snapshots_are_prefix_states():
+    q, k, v, z, beta, A = _rand(407, 2, 8, seed=31)
+    cu = np.array([0, 0, 130, 150, 343, 407], dtype=np.int32)   # lengths 0, 130, 20, 193, 64
+    S0 = np.random.default_rng(32).standard_normal((5, 2, 8, 8))
+    o, S_T, _, snaps = oracle.prefill(q, k, v, z, beta, A, cu_seqlens=cu, S0=S0, snap_interval=64)
+    assert snaps.shape == (2 + 0 + 3 + 1, 2, 8, 8)
+    row = 0
+    for n in range(5):
+        s, e = int(cu[n]), int(cu[n + 1])
+        for j in range(1, (e - s) // 64 + 1):
+            b = s + 64 * j
+            _, Sp, _ = oracle.prefill(q[s:b], k[s:b], v[s:b], z[s:b], beta[s:b], A, S0=S0[n:n + 1])
+            assert np.array_equal(snaps[row], Sp[0]), (n, j)
+            o_rest, S_rest, _ = oracle.prefill(q[b:e], k[b:e], v[b:e], z[b:e], beta[b:e], A,
+                                               S0=snaps[row:row + 1])
+            assert np.array_equal(o_rest, o[b:e]) and np.array_equal(S_rest[0], S_T[n])
+            row += 1
+    assert row == snaps.shape[0]
+    # the sequence of length 64 ends on a boundary: its one snapshot is its final state
+    assert np.array_equal(snaps[-1], S_T[4])
+    # snapshots leave the other outputs unchanged
+    o2, S2, _ = oracle.prefill(q, k, v, z, beta, A, cu_seqlens=cu, S0=S0)
+    assert np.array_equal(o, o2) and np.array_equal(S_T, S2)
+
+
+# --------------------------------------------------------------------------
 # Mutation check: plant slips in a copy of the C oracle; the pins must notice
 # --------------------------------------------------------------------------
 
@@ -311,6 +343,10 @@ MUTATIONS = {
     "sign_of_delta": ("u[j] = bt * (vt[j] - u[j]);", "u[j] = bt * (vt[j] + u[j]);"),
     "transposed_readout": ("ot[j] += S[(size_t)i * dv + j] * qn[i];", "ot[j] += S[(size_t)j * dv + i] * qn[i];"),
     "gate_sign": ("return g_min * sigmoid(exp(A_h) * z);", "return g_min * sigmoid(-exp(A_h) * z);"),
+    "snapshot_one_token_early": ("(t + 1 - cu_seqlens[n]) % snap_interval == 0",
+                                 "(t + 2 - cu_seqlens[n]) % snap_interval == 0"),
+    "snapshot_rows_restart": ("snap_row += (cu_seqlens[m + 1] - cu_seqlens[m]) / snap_interval;",
+                              "snap_row += 0;"),
 }
 
 
@@ -336,7 +372,8 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         oracle._lib = lib
         failed = False
         for pin in (lambda: test_brute_force_rational(4, 4), test_delta_invariant,
-                    test_gate_closed_forms, lambda: test_chunked_equals_recurrence(150, 64, 16)):
+                    test_gate_closed_forms, lambda: test_chunked_equals_recurrence(150, 64, 16),
+                    test_snapshots_are_prefix_states):
             try:
                 pin()
             except AssertionError:
