@@ -82,9 +82,21 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *
  * Supported: dk = dv = 128 with bf16 q/k/v (tensor-core chunked path), and
  * dk = dv in {32, 64, 128} with float32 q/k/v (CUDA-core path); H >= 1.
- * workspace: device scratch of kda_prefill_workspace_size() bytes (may be
- * NULL when that size is 0).
+ * workspace: device scratch.  On the tensor-core path the size selects the
+ * schedule:
+ *  - workspace_bytes >= kda_prefill_workspace_size(): chunk-parallel schedule
+ *    (one pass over all (chunk, head) pairs in parallel writes each chunk's
+ *    state-free terms, 160.5 KiB per chunk and head, to the workspace; a second
+ *    pass runs the state recurrence per (sequence, head)).  The fastest.
+ *  - KDA_PREFILL_MIN_WORKSPACE <= workspace_bytes < that: single-pass schedule
+ *    (one cluster per (sequence, head) walks its chunks); no scratch beyond
+ *    the error word.
+ *  - less: KDA_ERR_WORKSPACE.
+ * The first 4 bytes of the workspace are an error word: a wait inside a
+ * kernel that gave up ORs 1 into it (zero it before the call to read it).
+ * The CUDA-core path needs no workspace (size 0; may be NULL).
  */
+#define KDA_PREFILL_MIN_WORKSPACE 256
 typedef struct {
     int num_seqs;
     int T_total;
@@ -144,9 +156,10 @@ kda_status kda_prefill(const kda_prefill_args* args, void* stream);
  * array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's own device memory
  * (every GPU that loads the library holds it until the process exits).  It
  * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *  - Calls whose scratch requirement (kda_prefill_workspace_size) exceeds
- *    KDA_NOALLOC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE (the
- *    message is in kda_last_error_string()).
+ *  - It runs the schedule that needs the least scratch (on the tensor-core
+ *    path the single-pass one, KDA_PREFILL_MIN_WORKSPACE bytes); calls whose
+ *    least scratch exceeds KDA_NOALLOC_SCRATCH_BYTES are rejected with
+ *    KDA_ERR_WORKSPACE (the message is in kda_last_error_string()).
  *  - All calls share the one array; it keeps the previous call's contents and
  *    each call clears what must start at zero (with cudaMemsetAsync on the
  *    caller's stream).  Calls that overlap on the GPU (different streams with

@@ -16,6 +16,8 @@ size_t prefill_noalloc_scratch_needed(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc_noalloc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_tc_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
+size_t prefill_split_workspace_size(const kda_prefill_args& a);
+cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s);
 }  // namespace kda
 
 static thread_local char g_last_error[256] = "no error";
@@ -97,7 +99,7 @@ long kda_prefill_snapshot_count(const kda_prefill_args* a) {
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
     if (validate_prefill(a) != KDA_OK) return 0;
-    if (kda::prefill_tc_supported(*a)) return kda::prefill_tc_workspace_size(*a);
+    if (kda::prefill_tc_supported(*a)) return kda::prefill_split_workspace_size(*a);
     return 0;
 }
 
@@ -108,9 +110,12 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (kda::prefill_tc_supported(*a)) {
-        if (a->workspace_bytes < kda::prefill_tc_workspace_size(*a)) return KDA_ERR_WORKSPACE;
-        if (a->workspace_bytes > 0 && !a->workspace) return KDA_ERR_WORKSPACE;
-        e = kda::launch_prefill_tc(*a, s);
+        if (!a->workspace || a->workspace_bytes < KDA_PREFILL_MIN_WORKSPACE) return KDA_ERR_WORKSPACE;
+        if (misaligned(a->workspace)) return KDA_ERR_ALIGN;
+        if (a->workspace_bytes >= kda::prefill_split_workspace_size(*a))
+            e = kda::launch_prefill_split(*a, s);
+        else
+            e = kda::launch_prefill_tc(*a, s);
     } else {
         e = kda::launch_prefill_recurrent(*a, s);
     }

@@ -1,0 +1,1054 @@
+// Chunk-parallel KDA prefill on the sm_103a tensor cores: the state-free part
+// of every chunk runs in parallel over all chunks, and only the state recurrence
+// runs sequentially.
+//
+// Operator: "Kimi K3: KDA, attention residuals and Stable LatentMoE"
+// (hs-black.github.io) Sec. 2.1 chunked form with the Sec. 2.2 bounded gate and
+// 16-token sub-chunks and the Sec. 2.3 output gate.  Per chunk of C = 64 tokens
+// (notation as in the single-pass kernel):
+//   [U | W ; U_o | P Gamma K] = [T Diag(beta) ; P Diag(beta)] . [V | Gamma K]
+//   [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S
+//   S_next   = Diag(gamma_C) S + (K gamma_C / Gamma)^T V'
+// Everything in the first line, and the operands of the other two, depends on
+// the chunk's own tokens only.  Unrolled over chunks, the state obeys
+//   S_{c+1} = E_c S_c + F_c,  E_c = Diag(gamma_C) - (K gamma_C/Gamma)^T W,
+//                             F_c = (K gamma_C/Gamma)^T U,
+// which is the per-segment transition pair of the pages' context parallelism
+// (Sec. 10.2: S_exit = M S_entry + S~) at the granularity of one chunk, kept in
+// factored (rank-64) form so that applying it costs two thin products.
+//
+// Three launches on the caller's stream:
+//   plan  -- chunk offsets of the packed sequences (exclusive scan of
+//            ceil(len / 64)) into the workspace;
+//   prep  -- persistent, one CTA per SM, a loop over (chunk, head) records:
+//            gate, Gram sub-blocks, blockwise UT solve and MMA 1 (the same
+//            arithmetic as the single-pass kernel), then writes the record
+//            [-W ; Gamma Q - P Gamma K] (tf32 values), [U ; U_o] (fp32),
+//            (K gamma_C / Gamma)^T (tf32 values) and gamma_C;
+//   scan  -- a cluster of two CTAs per (sequence, head), CTA r owning value
+//            columns [64r, 64r+64): per chunk MMA 2 (A from shared memory by
+//            TMA, accumulating onto [U ; U_o] preloaded into TMEM), V' to the
+//            MMA 3 operand, O to o and the fused output gate, MMA 3, and the
+//            FP32 state update in TMEM.  The records of the next chunks are
+//            fetched while the current one is processed.
+#include <mutex>
+
+#include "kda_common.cuh"
+#include "tcgen05.cuh"
+#include "tma_host.cuh"
+
+namespace kda {
+namespace spl {
+
+constexpr int C = 64;     // chunk length
+constexpr int D = 128;    // dk = dv
+constexpr int NT = 256;   // threads per CTA
+constexpr int QS = 132;   // padded row stride (floats) of the scaled q/k tiles
+constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
+constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
+constexpr int NE = 64;    // scan: value columns per CTA
+
+// one record per (chunk, head), in four arrays of the workspace
+constexpr size_t AW_FLOATS = 128 * 128;   // [-W ; Gamma Q - P Gamma K]  [row][d]
+constexpr size_t UU_FLOATS = 128 * 128;   // [U ; U_o]                   [row][e]
+constexpr size_t KT_FLOATS = 128 * 64;    // (K gamma_C / Gamma)^T       [d][t]
+constexpr size_t GM_FLOATS = 128;         // gamma_C                     [d]
+
+struct Work {
+    const int* chunk_base;   // [num_seqs + 1] first global chunk of each sequence
+    float* aw;
+    float* uu;
+    float* kt;
+    float* gm;
+    int* err;                // bounded waits that gave up set bit 0
+    long nrec;               // chunks * H
+};
+
+TC_DEV uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_u32(p)), "r"(rank));
+    return r;
+}
+TC_DEV void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+}
+TC_DEV void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// byte offset of bf16 element (row, col) in a [rows][64] tile written by TMA with the 128-B swizzle
+TC_DEV uint32_t sw128_bf16(int row, int col) {
+    return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+}
+TC_DEV float4 ld_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+// After a wait gave up anywhere in the CTA, give copies still in flight into
+// this CTA's shared memory about a millisecond to land before it is released.
+TC_DEV void drain_if(bool timed_out) {
+    if (__syncthreads_or(timed_out) && threadIdx.x == 0)
+        for (int i = 0; i < 1000; ++i) __nanosleep(1000);
+}
+
+// ---------------------------------------------------------------------------
+// plan: chunk_base[n] = sum_{m < n} ceil(len_m / C), n = 0..num_seqs (one CTA)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs, int* chunk_base) {
+    __shared__ int s_warp[32];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < num_seqs; base += 1024) {
+        const int n = base + tid;
+        const int v = n < num_seqs ? (cu[n + 1] - cu[n] + C - 1) / C : 0;
+        int x = v;   // inclusive scan inside the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = s_warp[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int carry = s_carry;
+        const int incl = carry + x + (warp > 0 ? s_warp[warp - 1] : 0);
+        if (n < num_seqs) chunk_base[n] = incl - v;
+        __syncthreads();
+        if (tid == 1023) s_carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_base[num_seqs] = s_carry;
+}
+
+// record -> (sequence, first token, tokens, head); chunk_base has num_seqs + 1 entries
+struct Loc { int t0, nc, h; };
+TC_DEV Loc locate(long rec, int H, const int* cu, const int* cb, int num_seqs) {
+    const int g = (int)(rec / H);
+    Loc l;
+    l.h = (int)(rec - (long)g * H);
+    int lo = 0, hi = num_seqs;          // largest n with cb[n] <= g (cb[num_seqs] > g)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cb[mid] <= g) lo = mid; else hi = mid;
+    }
+    l.t0 = cu[lo] + C * (g - cb[lo]);
+    l.nc = min(C, cu[lo + 1] - l.t0);
+    return l;
+}
+
+// ---------------------------------------------------------------------------
+// prep: the state-free part of every chunk
+// ---------------------------------------------------------------------------
+namespace prep {
+constexpr int RB_BYTES = 65536;                     // raw q,k,z | Gram tiles | [V | Gamma K]^T
+constexpr int TILE_BYTES = C * QS * 4;
+constexpr int OFF_RB = 0;
+constexpr int OFF_RAWQ = OFF_RB;                    // [C][D] bf16
+constexpr int OFF_RAWK = OFF_RB + C * D * 2;        // [C][D] bf16
+constexpr int OFF_RAWZ = OFF_RB + 2 * C * D * 2;    // [C][D] f32
+constexpr int OFF_AQK = OFF_RB;
+constexpr int OFF_AKK = OFF_RB + C * AS * 4;
+constexpr int OFF_BPRE = OFF_RB;                    // SW128 [256 rows][C]
+constexpr int OFF_QH = OFF_RB + RB_BYTES;
+constexpr int OFF_KR = OFF_QH + TILE_BYTES;
+constexpr int OFF_KH = OFF_KR + TILE_BYTES;
+constexpr int OFF_RAWV = OFF_KH + TILE_BYTES;       // two [C][64] bf16 tiles, 128-B swizzle
+constexpr int OFF_SMALL = OFF_RAWV + 2 * C * 64 * 2;
+constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
+              SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
+              SM_FLOATS = SM_CTAB + NPAIR * D;
+constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
+static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0, "swizzled tiles need 1024-B alignment");
+static_assert(2 * D * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
+static_assert(3 * C * AS * 4 + (NT / 32) * 16 * 16 * 4 <= RB_BYTES, "region RB holds the solve tiles");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;
+constexpr uint32_t BYTES_V = C * D * 2;
+constexpr uint32_t TM_D = 0;     // 256 cols: [U | W ; U_o | P Gamma K]
+constexpr uint32_t TM_A2 = 256;  // 64 cols: [T beta ; P beta]
+constexpr uint32_t TM_COLS = 512;
+}  // namespace prep
+
+__global__ void __launch_bounds__(NT, 1)
+prep_kernel(kda_prefill_args a, Work w,
+            const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v) {
+    using namespace prep;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sBpre = sm + OFF_BPRE;
+    const uint16_t* sRawQ = reinterpret_cast<const uint16_t*>(sm + OFF_RAWQ);
+    const uint16_t* sRawK = reinterpret_cast<const uint16_t*>(sm + OFF_RAWK);
+    const float* sRawZ = reinterpret_cast<const float*>(sm + OFF_RAWZ);
+    const uint8_t* sRawV = sm + OFF_RAWV;
+    float* sQ = reinterpret_cast<float*>(sm + OFF_QH);
+    float* sKr = reinterpret_cast<float*>(sm + OFF_KR);
+    float* sK = reinterpret_cast<float*>(sm + OFF_KH);
+    float* sAqk = reinterpret_cast<float*>(sm + OFF_AQK);
+    float* sAkk = reinterpret_cast<float*>(sm + OFF_AKK);
+    float* fs = reinterpret_cast<float*>(sm + OFF_SMALL);
+    float* s_beta = fs + SM_BETA;
+    float* s_rq = fs + SM_RQ;
+    float* s_rk = fs + SM_RK;
+    float* s_tau = fs + SM_TAU;
+    float* s_expS = fs + SM_EXPS;
+    float* s_expCE = fs + SM_EXPCE;
+    float* s_gam = fs + SM_GAM;
+    float* s_ctab = fs + SM_CTAB;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
+    uint64_t* bar_in = mbar + 1;
+    uint64_t* bar_v = mbar + 2;
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 3);
+
+    const int H = a.H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hf = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int c_lo = hf * 32;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const long stride = gridDim.x;
+    long rec = blockIdx.x;
+    Loc cur = locate(rec, H, a.cu_seqlens, w.chunk_base, a.num_seqs);
+
+    if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        tc::mbar_init(bar_in, 1);
+        tc::mbar_init(bar_v, 1);
+        tc::mbar_fence_init();
+        tc::tma_prefetch_desc(&tm_q);
+        tc::tma_prefetch_desc(&tm_k);
+        tc::tma_prefetch_desc(&tm_z);
+        tc::tma_prefetch_desc(&tm_v);
+        if (rec < w.nrec) {
+            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
+            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, cur.h * D, cur.t0, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, cur.h * D, cur.t0, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, cur.h * D, cur.t0, bar_in);
+            tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
+            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, cur.h * D, cur.t0, bar_v);
+            tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, cur.h * D + 64, cur.t0, bar_v);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t T0 = *tbase_ptr;
+    uint32_t ph_mma = 0, ph_in = 0, ph_v = 0;
+    bool timed_out = false;
+    // a wait that gives up records it, and every later wait is skipped so that
+    // the kernel runs to its end quickly (its results are then invalid)
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
+    };
+    float beta_next = 0.f;
+    if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
+
+    for (; rec < w.nrec; rec += stride) {
+        const long nrec_next = rec + stride;
+        const bool has_next = nrec_next < w.nrec;
+        const Loc nxt = has_next ? locate(nrec_next, H, a.cu_seqlens, w.chunk_base, a.num_seqs) : cur;
+        const int nc = cur.nc, h = cur.h;
+        const float eA = __expf(a.A[h]);
+        if (tid < C) {
+            s_beta[tid] = beta_next;
+            beta_next = (has_next && tid < nxt.nc) ? a.beta[(size_t)(nxt.t0 + tid) * H + nxt.h] : 0.f;
+        }
+        wait(bar_in, ph_in);
+        ph_in ^= 1u;
+
+        // ---- 1a. q/k L2 norms (warp w: tokens 8w..8w+7)
+#pragma unroll 4
+        for (int i = 0; i < 8; ++i) {
+            const int t = warp * 8 + i;
+            float sq = 0.f, sk = 0.f;
+            if (t < nc) {
+                const uint2 qa = *reinterpret_cast<const uint2*>(sRawQ + t * D + 4 * lane);
+                const uint2 ka = *reinterpret_cast<const uint2*>(sRawK + t * D + 4 * lane);
+                const float q0 = __uint_as_float(qa.x << 16), q1 = __uint_as_float(qa.x & 0xffff0000u),
+                            q2 = __uint_as_float(qa.y << 16), q3 = __uint_as_float(qa.y & 0xffff0000u);
+                const float k0 = __uint_as_float(ka.x << 16), k1 = __uint_as_float(ka.x & 0xffff0000u),
+                            k2 = __uint_as_float(ka.y << 16), k3 = __uint_as_float(ka.y & 0xffff0000u);
+                sq = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
+                sk = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            if (lane == 0) {
+                s_rq[t] = a.qk_l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+                s_rk[t] = a.qk_l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+            }
+        }
+        __syncthreads();
+
+        // ---- 1b. gate and sub-chunk-relative decay factors (channel d, sub-chunks 2hf, 2hf+1)
+        {
+            const int d = tid & (D - 1);
+#pragma unroll 1
+            for (int b = 2 * (tid >> 7); b < 2 * (tid >> 7) + 2; ++b) {
+                float al[16], kv[16];
+                float F1 = 1.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = 16 * b + i;
+                    float alpha = 1.f, q = 0.f, k = 0.f;
+                    if (t < nc) {
+                        alpha = __expf(log_decay(sRawZ[t * D + d], eA, a.g_min));
+                        q = bf16_to_f(sRawQ[t * D + d]) * s_rq[t];
+                        k = bf16_to_f(sRawK[t * D + d]) * s_rk[t];
+                    }
+                    F1 *= alpha;                   // exp(G_t - G_start(b))
+                    al[i] = alpha;
+                    kv[i] = k;
+                    sQ[t * QS + d] = q * F1;
+                    sKr[t * QS + d] = k * F1;
+                }
+                float F2 = 1.f;                    // exp(G_end(b) - G_t)
+#pragma unroll
+                for (int i = 15; i >= 0; --i) {
+                    sK[(16 * b + i) * QS + d] = kv[i] * F2;
+                    F2 *= al[i];
+                }
+                s_tau[b * D + d] = F1;
+            }
+        }
+        __syncthreads();   // raw q/k/z are dead from here on
+        if (tid < D) {
+            const int d = tid;
+            float tau[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tau[b] = s_tau[b * D + d];
+            float pre = 1.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) { s_expS[b * D + d] = pre; pre *= tau[b]; }
+            s_gam[d] = pre;
+            float suf = 1.f;
+#pragma unroll
+            for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= tau[b]; }
+#pragma unroll
+            for (int aa = 0; aa < 4; ++aa) {
+#pragma unroll
+                for (int bb = 0; bb <= aa; ++bb) {
+                    float cf = 1.f;
+                    if (aa == bb) cf = __fdividef(1.f, tau[aa]);
+                    else {
+#pragma unroll
+                        for (int m = bb + 1; m < aa; ++m) cf *= tau[m];
+                    }
+                    s_ctab[(aa * (aa + 1) / 2 + bb) * D + d] = cf;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- 2. Gram sub-blocks, mma.sync tf32: blocks 0..9 of A_qk, 10..19 of A_kk;
+        //         warp w owns blocks w, w+8, w+16
+        {
+            const int g = lane >> 2, t4 = lane & 3;
+            float acc[3][2][4];
+#pragma unroll
+            for (int it = 0; it < 3; ++it)
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
+            int ia[3], ib[3];
+            bool kk[3], on[3];
+#pragma unroll
+            for (int it = 0; it < 3; ++it) {
+                const int blk_id = warp + 8 * it;
+                on[it] = blk_id < 2 * NPAIR;
+                kk[it] = blk_id >= NPAIR;
+                const int pr = kk[it] ? blk_id - NPAIR : blk_id;
+                const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
+                ia[it] = aa;
+                ib[it] = pr - aa * (aa + 1) / 2;
+            }
+#pragma unroll 2
+            for (int ks = 0; ks < 16; ++ks) {
+                const int k0 = 8 * ks + t4, k1 = k0 + 4;
+#pragma unroll
+                for (int it = 0; it < 3; ++it) {
+                    if (on[it]) {
+                        const float* Arows = kk[it] ? sKr : sQ;
+                        const int ra = 16 * ia[it] + g;
+                        const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
+                                             tc::to_tf32(Arows[ra * QS + k1]), tc::to_tf32(Arows[(ra + 8) * QS + k1])};
+                        const float* ct = s_ctab + (ia[it] * (ia[it] + 1) / 2 + ib[it]) * D;
+                        const float c0f = ct[k0], c1f = ct[k1];
+#pragma unroll
+                        for (int nh = 0; nh < 2; ++nh) {
+                            const int j = 16 * ib[it] + 8 * nh + g;
+                            const float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
+                            tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < 3; ++it) {
+                if (on[it]) {
+                    float* Out = kk[it] ? sAkk : sAqk;
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh) {
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int I = 16 * ia[it] + g + 8 * hr;
+                            const int J = 16 * ib[it] + 8 * nh + 2 * t4;
+                            float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
+                            if (!kk[it]) { if (J > I) v0 = 0.f; if (J + 1 > I) v1 = 0.f; }
+                            else {
+                                const float bI = s_beta[I];
+                                v0 = (J >= I) ? 0.f : v0 * bI;
+                                v1 = (J + 1 >= I) ? 0.f : v1 * bI;
+                            }
+                            *reinterpret_cast<float2*>(Out + I * AS + J) = make_float2(v0, v1);
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- 3. blockwise UT solve: T = (I + A_kk)^{-1}, P = A_qk T (16x16 blocks)
+        {
+            float* sT = sAkk + C * AS;
+            float* sW = sT + C * AS;
+            const int g = lane >> 2, t4 = lane & 3;
+            float* wsc = sW + warp * 16 * 16;
+            auto blk = [&](float* M, int a_, int b_) { return M + (16 * a_) * AS + 16 * b_; };
+            auto mma16 = [&](float (&acc)[2][4], const float* X, const float* Y, int ly) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks + t4, k1 = k0 + 4;
+                    const float af[4] = {tc::to_tf32(X[g * AS + k0]), tc::to_tf32(X[(g + 8) * AS + k0]),
+                                         tc::to_tf32(X[g * AS + k1]), tc::to_tf32(X[(g + 8) * AS + k1])};
+#pragma unroll
+                    for (int nh = 0; nh < 2; ++nh) {
+                        const int nn = 8 * nh + g;
+                        const float bfr[2] = {tc::to_tf32(Y[k0 * ly + nn]), tc::to_tf32(Y[k1 * ly + nn])};
+                        tc::mma_m16n8k8_tf32(acc[nh], af, bfr);
+                    }
+                }
+            };
+            auto zero = [&](float (&acc)[2][4]) {
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) acc[nh][q4] = 0.f;
+            };
+            auto store = [&](const float (&acc)[2][4], float* Y, int ly, float sgn) {
+#pragma unroll
+                for (int nh = 0; nh < 2; ++nh)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        Y[(g + (q4 >= 2 ? 8 : 0)) * ly + 8 * nh + 2 * t4 + (q4 & 1)] = sgn * acc[nh][q4];
+            };
+            auto t_block = [&](int a_, int b_) {
+                float acc[2][4];
+                zero(acc);
+#pragma unroll 1
+                for (int c_ = b_; c_ < a_; ++c_) mma16(acc, blk(sAkk, a_, c_), blk(sT, c_, b_), AS);
+                store(acc, wsc, 16, 1.f);
+                __syncwarp();
+                float acc2[2][4];
+                zero(acc2);
+                mma16(acc2, blk(sT, a_, a_), wsc, 16);
+                store(acc2, blk(sT, a_, b_), AS, -1.f);
+                __syncwarp();
+            };
+            auto p_block = [&](float (&acc)[2][4], int a_, int b_) {
+                zero(acc);
+#pragma unroll 1
+                for (int c_ = b_; c_ <= a_; ++c_) mma16(acc, blk(sAqk, a_, c_), blk(sT, c_, b_), AS);
+            };
+            if (tid < C) {
+                const int aa = tid >> 4, i = tid & 15;
+                const float* Ad = blk(sAkk, aa, aa);
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = (j == i) ? 1.f : 0.f;
+#pragma unroll
+                for (int kk = 15; kk >= 1; --kk) {
+                    const float xk = x[kk];
+#pragma unroll
+                    for (int j = 0; j < kk; ++j) x[j] = fmaf(-xk, Ad[kk * AS + j], x[j]);
+                }
+                float* Td = blk(sT, aa, aa) + i * AS;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) Td[j] = x[j];
+            }
+            __syncthreads();
+            float pA[2][4], pB[2][4];
+            if (warp < 3) t_block(warp + 1, warp);
+            else if (warp < 7) p_block(pA, warp - 3, warp - 3);
+            __syncthreads();
+            if (warp < 2) t_block(warp + 2, warp);
+            else if (warp == 2) p_block(pA, 2, 1);
+            else if (warp == 3) p_block(pB, 3, 2);
+            else if (warp == 7) p_block(pA, 1, 0);
+            __syncthreads();
+            if (warp == 0) t_block(3, 0);
+            else if (warp == 4) p_block(pB, 2, 0);
+            else if (warp == 5) p_block(pB, 3, 1);
+            __syncthreads();
+            if (warp == 6) p_block(pB, 3, 0);
+            __syncthreads();
+            switch (warp) {
+                case 2: store(pA, blk(sAqk, 2, 1), AS, 1.f); break;
+                case 3: store(pA, blk(sAqk, 0, 0), AS, 1.f); store(pB, blk(sAqk, 3, 2), AS, 1.f); break;
+                case 4: store(pA, blk(sAqk, 1, 1), AS, 1.f); store(pB, blk(sAqk, 2, 0), AS, 1.f); break;
+                case 5: store(pA, blk(sAqk, 2, 2), AS, 1.f); store(pB, blk(sAqk, 3, 1), AS, 1.f); break;
+                case 6: store(pA, blk(sAqk, 3, 3), AS, 1.f); store(pB, blk(sAqk, 3, 0), AS, 1.f); break;
+                case 7: store(pA, blk(sAqk, 1, 0), AS, 1.f); break;
+                default: break;
+            }
+            __syncthreads();
+            // rows of [T ; P] scaled by beta on the columns -> TMEM operand A2
+            const int i = row & 63;
+            const float* src = (row < C ? sT : sAqk) + i * AS;
+            float v[16];
+#pragma unroll
+            for (int c = c_lo; c < c_lo + C / 2; c += 16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int col = c + j;
+                    v[j] = (col <= i) ? tc::to_tf32(src[col] * s_beta[col]) : 0.f;
+                }
+                tc::tmem_st16(T0 + TM_A2 + lane_base + c, v);
+            }
+        }
+        __syncthreads();   // the Gram tiles are dead from here on
+        wait(bar_v, ph_v);
+        ph_v ^= 1u;
+
+        // ---- 4. B_pre = [V | Gamma K]^T (256 rows), the record's (K gamma_C/Gamma)^T and gamma_C
+        {
+            if (tid < D) {                       // rows 0..127: value columns
+                const int e = tid;
+                const uint8_t* vt = sRawV + (e >> 6) * (C * 128);
+#pragma unroll 4
+                for (int t = 0; t < C; t += 4) {
+                    float4 w4;
+                    float* wp = &w4.x;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        wp[u] = (t + u < nc) ? bf16_to_f(*reinterpret_cast<const uint16_t*>(vt + sw128_bf16(t + u, e & 63)))
+                                             : 0.f;
+                    *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, 2 * D)) = w4;
+                }
+                w.gm[rec * GM_FLOATS + e] = s_gam[e];
+            } else {                             // rows 128..255: (Gamma K)^T
+                const int d = tid - D;
+#pragma unroll 4
+                for (int t = 0; t < C; t += 4) {
+                    float4 w4;
+                    float* wp = &w4.x;
+                    const float es = s_expS[(t >> 4) * D + d];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(sKr[(t + u) * QS + d] * es);
+                    *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(D + d, t, 2 * D)) = w4;
+                }
+            }
+            const int d = row;                   // (K gamma_C / Gamma)^T: row d, 32 token columns
+            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + c_lo;
+#pragma unroll
+            for (int t = 0; t < C / 2; t += 4) {
+                const int tt = c_lo + t;
+                const float ec = s_expCE[(tt >> 4) * D + d];
+                st_stream_f4(dst + t, make_float4(tc::to_tf32(sK[tt * QS + d] * ec), tc::to_tf32(sK[(tt + 1) * QS + d] * ec),
+                                                  tc::to_tf32(sK[(tt + 2) * QS + d] * ec), tc::to_tf32(sK[(tt + 3) * QS + d] * ec)));
+            }
+            tc::tmem_st_wait();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+        }
+        __syncthreads();
+        // the raw v tiles are consumed: fetch the next record's
+        if (tid == 0 && has_next) {
+            tc::fence_proxy_async();
+            tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
+            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, nxt.h * D, nxt.t0, bar_v);
+            tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, nxt.h * D + 64, nxt.t0, bar_v);
+        }
+
+        // ---- 5. MMA 1: D[:, 0:256] = [T beta ; P beta] . [V | Gamma K]
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t bb = tc::smem_u32(sBpre);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(T0 + TM_D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bb, 2 * D, ks),
+                                tc::idesc_tf32(128, 2 * D), ks > 0);
+            tc::mma_commit(mbar);
+        }
+        wait(mbar, ph_mma);
+        ph_mma ^= 1u;
+        tc::fence_after_sync();
+        // region RB is free again: fetch the next record's q, k, z into it
+        if (tid == 0 && has_next) {
+            tc::fence_proxy_async();
+            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
+            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, nxt.h * D, nxt.t0, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, nxt.h * D, nxt.t0, bar_in);
+            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, nxt.h * D, nxt.t0, bar_in);
+        }
+
+        // ---- 6. the record: [U ; U_o] and [-W ; Gamma Q - P Gamma K] (row = lane, 64 columns)
+        {
+            float v[16];
+            float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 64 * hf;
+            float* aw = w.aw + rec * AW_FLOATS + (size_t)row * D + 64 * hf;
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 16) {
+                tc::tmem_ld16(T0 + TM_D + lane_base + 64 * hf + c, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) st_stream_f4(uu + c + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+            }
+            if (row < C) {
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 64 * hf + c, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        st_stream_f4(aw + c + j, make_float4(tc::to_tf32(-v[j]), tc::to_tf32(-v[j + 1]),
+                                                             tc::to_tf32(-v[j + 2]), tc::to_tf32(-v[j + 3])));
+                }
+            } else {
+                const int t = row - C;
+                const float* es = s_expS + (t >> 4) * D;
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 64 * hf + c, v);
+                    tc::tmem_ld_wait();
+                    float o4[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int d = 64 * hf + c + j;
+                        o4[j] = tc::to_tf32(sQ[t * QS + d] * es[d] - v[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) st_stream_f4(aw + c + j, make_float4(o4[j], o4[j + 1], o4[j + 2], o4[j + 3]));
+                }
+            }
+            tc::fence_before_sync();
+        }
+        __syncthreads();
+        cur = nxt;
+    }
+    if (timed_out && w.err) atomicOr(w.err, 1);
+    drain_if(timed_out);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// scan: the state recurrence over one sequence's records
+// ---------------------------------------------------------------------------
+namespace scan {
+constexpr int AW_TILE = 128 * 128 * 4;              // SW128 [128 rows][128 K]
+constexpr int OFF_AW0 = 0;
+constexpr int OFF_AW1 = AW_TILE;
+constexpr int OFF_SOP = 2 * AW_TILE;                // S operand, SW128 [e][d]        32 KB
+constexpr int OFF_VOP = OFF_SOP + NE * D * 4;       // V' operand, SW128 [e][t]       16 KB
+constexpr int OFF_G0 = OFF_VOP + NE * C * 4;        // g_in tiles, [C][64] bf16 swizzled
+constexpr int OFF_G1 = OFF_G0 + C * NE * 2;
+constexpr int OFF_SMALL = OFF_G1 + C * NE * 2;
+constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * C, SM_FLOATS = 4 * C;
+constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
+static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0 && OFF_G1 % 1024 == 0,
+              "swizzled tiles need 1024-B alignment");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr uint32_t TM_D = 0;      // 2 x 64 cols: [U ; U_o] -> [V' ; O], by chunk parity
+constexpr uint32_t TM_A3 = 128;   // 2 x 64 cols: (K gamma_C / Gamma)^T, by chunk parity
+constexpr uint32_t TM_DS = 256;   // 64 cols: state increment
+constexpr uint32_t TM_S = 320;    // 64 cols: FP32 state
+constexpr uint32_t TM_COLS = 512;
+}  // namespace scan
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
+scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
+            const __grid_constant__ CUtensorMap tm_g) {
+    using namespace scan;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sSop = sm + OFF_SOP;
+    uint8_t* sVop = sm + OFF_VOP;
+    float* fs = reinterpret_cast<float*>(sm + OFF_SMALL);
+    float* s_rowsq = fs + SM_ROWSQ;      // [2][C] peer's row sums of squares (by chunk parity)
+    float* s_rowpart = fs + SM_ROWPART;  // [2][C] this CTA's, per column half
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
+    uint64_t* bar_aw = mbar + 1;         // [2]
+    uint64_t* bar_g = mbar + 3;          // [2]
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 5);
+
+    const int r = blockIdx.x;
+    const int h = blockIdx.y;
+    const int n = blockIdx.z;
+    const int H = a.H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, hf = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int c_lo = hf * (NE / 2);
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
+    const int g0 = w.chunk_base[n];
+    const int nch = w.chunk_base[n + 1] - g0;
+    const bool gate = a.g_in != nullptr;
+    auto rec_of = [&](int j) { return (long)(g0 + j) * H + h; };
+
+    if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
+    if (tid == 0) {
+        tc::mbar_init(mbar, 1);
+        for (int b = 0; b < 2; ++b) { tc::mbar_init(bar_aw + b, 1); tc::mbar_init(bar_g + b, 1); }
+        tc::mbar_fence_init();
+        tc::tma_prefetch_desc(&tm_aw);
+        if (gate) tc::tma_prefetch_desc(&tm_g);
+        for (int j = 0; j < 2 && j < nch; ++j) {
+            uint8_t* dst = sm + (j ? OFF_AW1 : OFF_AW0);
+            tc::mbar_arrive_expect_tx(bar_aw + j, AW_TILE);
+            for (int s = 0; s < 4; ++s)
+                tc::tma_load_2d(dst + s * (AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + j);
+            if (gate) {
+                tc::mbar_arrive_expect_tx(bar_g + j, C * NE * 2);
+                tc::tma_load_2d(sm + (j ? OFF_G1 : OFF_G0), &tm_g, h * D + NE * r, t_begin + C * j, bar_g + j);
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t T0 = *tbase_ptr;
+    uint32_t ph_mma = 0;
+    bool timed_out = false;
+    // a wait that gives up records it, and every later wait is skipped (the loop
+    // keeps its cluster barriers, so the peer CTA is never left waiting)
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
+    };
+    auto mma_wait = [&]() {
+        wait(mbar, ph_mma);
+        ph_mma ^= 1u;
+        tc::fence_after_sync();
+    };
+
+    // record loads into registers: [U ; U_o] row `row`, this CTA's 32 columns of
+    // this thread; (K gamma_C / Gamma)^T row `row`, tokens c_lo..c_lo+31
+    float4 pu[8], pk[8];
+    auto load_rec = [&](int j) {
+        const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
+        const float* k = w.kt + rec_of(j) * KT_FLOATS + (size_t)row * C + c_lo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { pu[i] = ld_f4(u + 4 * i); pk[i] = ld_f4(k + 4 * i); }
+    };
+    auto store_rec = [&](int b) {
+#pragma unroll
+        for (int i = 0; i < 8; i += 4) {
+            tc::tmem_st16(T0 + TM_D + 64 * b + lane_base + c_lo + 4 * i, reinterpret_cast<const float*>(pu + i));
+            tc::tmem_st16(T0 + TM_A3 + 64 * b + lane_base + c_lo + 4 * i, reinterpret_cast<const float*>(pk + i));
+        }
+    };
+
+    // ---- initial state -> TMEM master copy and the tf32 operand copy
+    {
+        const int d = row;
+        const size_t sb = (((size_t)n * H + h) * D + d) * D + NE * r;
+        float v[16];
+#pragma unroll
+        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = a.S0 ? a.S0[sb + c + j] : 0.f;
+            tc::tmem_st16(T0 + TM_S + lane_base + c, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + j, d, NE)) = tc::to_tf32(v[j]);
+        }
+        if (nch > 0) { load_rec(0); store_rec(0); }
+        if (nch > 1) load_rec(1);
+        tc::tmem_st_wait();
+        tc::fence_proxy_async();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+
+#pragma unroll 1
+    for (int j = 0; j < nch; ++j) {
+        const int b = j & 1;
+        const int c0 = t_begin + C * j;
+        const int nc = min(C, t_end - c0);
+        const long rec = rec_of(j);
+        const float gm = w.gm[rec * GM_FLOATS + row];
+
+        // ---- MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S
+        if (tid == 0) {
+            wait(bar_aw + b, (j >> 1) & 1);
+            tc::fence_after_sync();
+            const uint32_t ab = tc::smem_u32(sm + (b ? OFF_AW1 : OFF_AW0));
+            const uint32_t sb = tc::smem_u32(sSop);
+#pragma unroll
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_tf32_ss(T0 + TM_D + 64 * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
+                                tc::idesc_tf32(128, NE), 1);
+            tc::mma_commit(mbar);
+        }
+        // the next record's [U ; U_o] and (K gamma_C/Gamma)^T into the other TMEM buffers,
+        // then fetch the one after it
+        if (j + 1 < nch) store_rec(b ^ 1);
+        if (j + 2 < nch) load_rec(j + 2);
+        tc::tmem_st_wait();
+        mma_wait();
+        if (tid == 0 && j + 2 < nch) {   // the A tile of this chunk is consumed
+            tc::mbar_arrive_expect_tx(bar_aw + b, AW_TILE);
+            for (int s = 0; s < 4; ++s)
+                tc::tma_load_2d(sm + (b ? OFF_AW1 : OFF_AW0) + s * (AW_TILE / 4), &tm_aw, 32 * s,
+                                (int)(rec_of(j + 2) * 128), bar_aw + b);
+        }
+
+        // ---- V' -> operand (smem), O -> o, row sums of squares for the output gate
+        float o[NE / 2];
+        {
+            float v[16];
+            float ss = 0.f;
+            if (row < C) {
+                const int t = row;
+#pragma unroll
+                for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + 64 * b + lane_base + c, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + jj, t, C)) = tc::to_tf32(v[jj]);
+                }
+            } else {
+                const int t = row - C;
+#pragma unroll
+                for (int c = 0; c < NE / 2; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + 64 * b + lane_base + c_lo + c, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) { o[c + jj] = a.scale * v[jj]; ss += o[c + jj] * o[c + jj]; }
+                }
+                if (t < nc) {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+                    for (int c = 0; c < NE / 2; c += 8) store8_bf16(dst + c, o + c);
+                }
+                if (gate) s_rowpart[hf * C + t] = ss;
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+        }
+        __syncthreads();
+
+        // ---- MMA 3: dS = (K gamma_C / Gamma)^T . V'
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t vb = tc::smem_u32(sVop);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(T0 + TM_DS, T0 + TM_A3 + 64 * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
+                                tc::idesc_tf32(128, NE), ks > 0);
+            tc::mma_commit(mbar);
+        }
+
+        // ---- fused output gate (row RMS over both CTAs' columns), while MMA 3 runs
+        if (gate) {
+            const int par = j & 1;
+            if (row >= C && hf == 0) {
+                const int t = row - C;
+                st_cluster_f32(cluster_map(s_rowsq + par * C + t, r ^ 1), s_rowpart[t] + s_rowpart[C + t]);
+            }
+            cluster_sync_all();
+            if (row >= C) {
+                const int t = row - C;
+                wait(bar_g + b, (j >> 1) & 1);
+                if (t < nc) {
+                    const uint8_t* sG = sm + (b ? OFF_G1 : OFF_G0);
+                    const float tot = s_rowpart[t] + s_rowpart[C + t] + s_rowsq[par * C + t];
+                    const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
+                    uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+                    for (int c = 0; c < NE / 2; c += 8) {
+                        const uint4 g8 = *reinterpret_cast<const uint4*>(sG + sw128_bf16(t, c_lo + c));
+                        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                        float yv[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
+                            const float wn = a.norm_w ? a.norm_w[NE * r + c_lo + c + jj] : 1.f;
+                            yv[jj] = sigmoidf_fast(gv) * wn * o[c + jj] * rr;
+                        }
+                        store8_bf16(yp + c, yv);
+                    }
+                }
+            }
+        }
+
+        // ---- S = Diag(gamma_C) S + dS (FP32 in TMEM), refresh the tf32 operand copy;
+        //      a chunk that closes a prefix-cache interval also writes S out
+        mma_wait();
+        {
+            const int d = row;
+            float* snap = nullptr;
+            if (a.S_snap && (c0 + nc - t_begin) % a.snap_interval == 0) {
+                const long srow = snapshot_row_base(a.cu_seqlens, n, a.snap_interval) +
+                                  (c0 + nc - t_begin) / a.snap_interval - 1;
+                snap = a.S_snap + ((srow * H + h) * D + d) * D + NE * r;
+            }
+            float dv[16], sv[16];
+#pragma unroll
+            for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
+                tc::tmem_ld16(T0 + TM_DS + lane_base + c, dv);
+                tc::tmem_ld16(T0 + TM_S + lane_base + c, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
+                tc::tmem_st16(T0 + TM_S + lane_base + c, sv);
+                if (snap) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; jj += 4)
+                        *reinterpret_cast<float4*>(snap + c + jj) = make_float4(sv[jj], sv[jj + 1], sv[jj + 2], sv[jj + 3]);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(sv[jj]);
+            }
+            tc::tmem_st_wait();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+        }
+        __syncthreads();
+        // the g_in tile of this chunk is consumed: fetch the one two chunks ahead
+        if (tid == 0 && gate && j + 2 < nch) {
+            tc::fence_proxy_async();
+            tc::mbar_arrive_expect_tx(bar_g + b, C * NE * 2);
+            tc::tma_load_2d(sm + (b ? OFF_G1 : OFF_G0), &tm_g, h * D + NE * r, t_begin + C * (j + 2), bar_g + b);
+        }
+    }
+
+    // ---- final state
+    if (a.S_T) {
+        const int d = row;
+        float* dst = a.S_T + (((size_t)n * H + h) * D + d) * D + NE * r;
+        float v[16];
+#pragma unroll
+        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
+            tc::tmem_ld16(T0 + TM_S + lane_base + c, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4)
+                *reinterpret_cast<float4*>(dst + c + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+        }
+    }
+    if (timed_out && w.err) atomicOr(w.err, 1);
+    drain_if(timed_out);
+    tc::fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();   // no CTA leaves while its peer may still write to its shared memory
+    if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static long total_chunks(const kda_prefill_args& a) {
+    long c = 0;
+    for (int n = 0; n < a.num_seqs; ++n) c += (a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] + C - 1) / C;
+    return c;
+}
+
+struct Layout { size_t base, aw, uu, kt, gm, total; long nrec; };
+static Layout layout(const kda_prefill_args& a) {
+    Layout l;
+    l.nrec = total_chunks(a) * a.H;
+    l.base = 256;                                            // error word first
+    l.aw = align_up(l.base + 4 * (size_t)(a.num_seqs + 1), 1024);
+    l.uu = l.aw + (size_t)l.nrec * AW_FLOATS * 4;
+    l.kt = l.uu + (size_t)l.nrec * UU_FLOATS * 4;
+    l.gm = l.kt + (size_t)l.nrec * KT_FLOATS * 4;
+    l.total = l.gm + (size_t)l.nrec * GM_FLOATS * 4;
+    return l;
+}
+
+static int sm_count() {
+    static int count[256] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!count[dev]) cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev);
+    return count[dev];
+}
+
+}  // namespace spl
+
+size_t prefill_split_workspace_size(const kda_prefill_args& a) { return spl::layout(a).total; }
+
+cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(spl::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        spl::prep::SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(spl::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            spl::scan::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    if (a.num_seqs == 0) return cudaSuccess;
+    const spl::Layout L = spl::layout(a);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(a.workspace);
+    spl::Work w;
+    w.err = reinterpret_cast<int*>(ws);
+    w.chunk_base = reinterpret_cast<const int*>(ws + L.base);
+    w.aw = reinterpret_cast<float*>(ws + L.aw);
+    w.uu = reinterpret_cast<float*>(ws + L.uu);
+    w.kt = reinterpret_cast<float*>(ws + L.kt);
+    w.gm = reinterpret_cast<float*>(ws + L.gm);
+    w.nrec = L.nrec;
+
+    const uint64_t rowq = (uint64_t)a.H * spl::D;
+    const uint64_t rows = (uint64_t)a.T_total;
+    CUtensorMap mq, mk, mz, mv, mg, maw;
+    cudaError_t e;
+    if ((e = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, rowq, rows, spl::D, spl::C,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, rowq, rows, spl::D, spl::C,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, rowq, rows, spl::D, spl::C,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, rowq, rows, 64, spl::C,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, rowq, rows, spl::NE,
+                      spl::C, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.aw, 128, (uint64_t)L.nrec * 128, 32, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+
+    spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base));
+    int launched = 1;
+    if (L.nrec > 0) {
+        const int nsm = spl::sm_count();
+        const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
+        spl::prep_kernel<<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+        ++launched;
+    }
+    dim3 grid(2, a.H, a.num_seqs);
+    spl::scan_kernel<<<grid, spl::NT, spl::scan::SMEM_BYTES, s>>>(a, w, maw, mg);
+    ++launched;
+    count_launches(launched);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -31,13 +31,11 @@
 // tf32 (nearest) when staged; the gate, cumulative decays, the triangular
 // solve and the state carry stay FP32 (the state lives in TMEM in FP32 across
 // chunks and is only rounded for its copy used as an MMA operand).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "kda_common.cuh"
 #include "tcgen05.cuh"
+#include "tma_host.cuh"
 
 namespace kda {
 namespace tcp {
@@ -767,37 +765,6 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
 }
 
-// ---------------------------------------------------------------------------
-// host: TMA descriptors
-// ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess && q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D map over a [rows][row_elems] row-major tensor, box = box_cols x box_rows
-static cudaError_t make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr,
-                            uint64_t row_elems, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
-                            CUtensorMapSwizzle sw) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {row_elems, rows < 1 ? 1 : rows};
-    cuuint64_t strides[1] = {row_elems * esize};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 }  // namespace tcp
 
 bool prefill_tc_supported(const kda_prefill_args& a) {
@@ -820,15 +787,15 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s) {
     const uint64_t rows = (uint64_t)a.T_total;
     CUtensorMap mq, mk, mz, mv, mg;
     cudaError_t e;
-    if ((e = tcp::make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, row, rows, tcp::D, tcp::C,
+    if ((e = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, row, rows, tcp::D, tcp::C,
                            CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = tcp::make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, row, rows, tcp::D, tcp::C,
+    if ((e = make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, row, rows, tcp::D, tcp::C,
                            CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = tcp::make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, row, rows, tcp::D, tcp::C,
+    if ((e = make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, row, rows, tcp::D, tcp::C,
                            CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = tcp::make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, row, rows, tcp::NE, tcp::C,
+    if ((e = make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, row, rows, tcp::NE, tcp::C,
                            CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-    if ((e = tcp::make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, row, rows, tcp::NE,
+    if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, row, rows, tcp::NE,
                            tcp::C, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     dim3 grid(2, a.H, a.num_seqs);
     tcp::prefill_tc_kernel<<<grid, tcp::NT, tcp::SMEM_BYTES, s>>>(a, reinterpret_cast<int*>(a.workspace),

@@ -169,6 +169,9 @@ def prefill_raw(args: PrefillArgs, stream=None, recurrent: bool = False):
     _check(fn(ctypes.byref(args), _stream(stream)), "kda_prefill_recurrent" if recurrent else "kda_prefill")
 
 
+PREFILL_MIN_WORKSPACE = 256   # smallest workspace of the tensor-core path (single-pass schedule)
+
+
 def snapshot_count(cu_seqlens_host, interval: int) -> int:
     """Rows of the snapshot output for packed sequences (see kda.h)."""
     cu = [int(x) for x in cu_seqlens_host]
@@ -210,7 +213,9 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
     if not recurrent:
         need = prefill_workspace_size(args)
         if need > 0:
-            if workspace is None or workspace.numel() * workspace.element_size() < need:
+            # a caller's workspace is used as given: its size picks the schedule
+            # (>= need: chunk-parallel; >= PREFILL_MIN_WORKSPACE: single pass)
+            if workspace is None:
                 workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
             args.workspace = workspace.data_ptr()
             args.workspace_bytes = workspace.numel() * workspace.element_size()

@@ -71,6 +71,39 @@ def test_in_place_state(kda_lib, cuda_dev):
     check(run_gpu(kda, d, cuda_dev, alias_state=True), run_oracle(d))
 
 
+@pytest.mark.parametrize("cu", [[0, 700], [0, 0, 1, 64, 130, 130, 400, 1000], [0, 63, 128, 193]])
+def test_schedules_agree(kda_lib, cuda_dev, cu):
+    """Chunk-parallel (full workspace) and single-pass (minimal workspace)
+    schedules: both match the oracle, the error word stays 0, and the two agree
+    to rounding."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    H = 3
+    d = I.make_prefill(I.workload("prefill_128k", T=cu[-1], H=H))
+    d["cu_seqlens"] = np.array(cu, dtype=np.int32)
+    d["S0"] = (0.02 * np.random.default_rng(7).standard_normal((len(cu) - 1, H, 128, 128))).astype(np.float32)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    args = dict(cu_seqlens=to_dev(d["cu_seqlens"], cuda_dev), S0=to_dev(d["S0"], cuda_dev),
+                g_in=to_dev(d["g_in"], cuda_dev, True))
+    z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
+    cu_host = args["cu_seqlens"].cpu()          # kept alive: the args hold its address
+    probe = kda.make_prefill_args(q, k, v, z, beta, A, args["cu_seqlens"], cu_host, torch.empty_like(v))
+    need = kda.prefill_workspace_size(probe)
+    assert need > 4096
+    ws_full = torch.zeros(need, dtype=torch.uint8, device=cuda_dev)
+    ws_min = torch.zeros(kda.PREFILL_MIN_WORKSPACE, dtype=torch.uint8, device=cuda_dev)
+    res = {}
+    for name, ws in (("split", ws_full), ("single", ws_min)):
+        res[name] = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
+        torch.cuda.synchronize()
+        assert int(ws[:4].view(torch.int32).item()) == 0, name
+    ref = run_oracle(d)
+    for name in res:
+        check(res[name], ref)
+    a, b = res["split"], res["single"]
+    assert rel(host(a[0]), host(b[0])) < TOL_O and rel(host(a[1]), host(b[1])) < TOL_S
+    assert rel(host(a[2]), host(b[2])) < TOL_O
+
+
 def test_chunked_matches_recurrent_gpu(kda_lib, cuda_dev):
     import serving_kda_chunked_gated_gb300.kda as kda
     d = I.make_prefill(I.workload("prefill_128k", T=700, H=4))
