@@ -67,4 +67,17 @@ KDA_DEV void store8_bf16(uint16_t* p, const float* in) {
 KDA_DEV float4 ld_stream_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 KDA_DEV void st_stream_f4(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+// 32 bytes (8 floats) per thread in one access, a whole 32-B sector per lane when
+// lanes touch different rows; p must be 32-byte aligned.
+KDA_DEV void st_stream_f8(float* p, const float* v) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+KDA_DEV void ld_nc_f8(const float* p, float* v) {
+    asm("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
 }  // namespace kda

@@ -46,7 +46,7 @@ constexpr int NT = 256;   // threads per CTA
 constexpr int QS = 132;   // padded row stride (floats) of the scaled q/k tiles
 constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
 constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
-constexpr int NE = 64;    // scan: value columns per CTA
+constexpr int SCAN_R = 4; // scan: CTAs (value-column blocks) per (sequence, head)
 
 // one record per (chunk, head), in four arrays of the workspace
 constexpr size_t AW_FLOATS = 128 * 128;   // [-W ; Gamma Q - P Gamma K]  [row][d]
@@ -560,11 +560,12 @@ prep_kernel(kda_prefill_args a, Work w,
             const int d = row;                   // (K gamma_C / Gamma)^T: row d, 32 token columns
             float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + c_lo;
 #pragma unroll
-            for (int t = 0; t < C / 2; t += 4) {
-                const int tt = c_lo + t;
-                const float ec = s_expCE[(tt >> 4) * D + d];
-                st_stream_f4(dst + t, make_float4(tc::to_tf32(sK[tt * QS + d] * ec), tc::to_tf32(sK[(tt + 1) * QS + d] * ec),
-                                                  tc::to_tf32(sK[(tt + 2) * QS + d] * ec), tc::to_tf32(sK[(tt + 3) * QS + d] * ec)));
+            for (int t = 0; t < C / 2; t += 8) {
+                const float ec = s_expCE[((c_lo + t) >> 4) * D + d];
+                float k8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(sK[(c_lo + t + u) * QS + d] * ec);
+                st_stream_f8(dst + t, k8);
             }
             tc::tmem_st_wait();
             tc::fence_proxy_async();
@@ -610,8 +611,8 @@ prep_kernel(kda_prefill_args a, Work w,
             for (int c = 0; c < 64; c += 16) {
                 tc::tmem_ld16(T0 + TM_D + lane_base + 64 * hf + c, v);
                 tc::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) st_stream_f4(uu + c + j, make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+                st_stream_f8(uu + c, v);
+                st_stream_f8(uu + c + 8, v + 8);
             }
             if (row < C) {
 #pragma unroll 1
@@ -619,9 +620,9 @@ prep_kernel(kda_prefill_args a, Work w,
                     tc::tmem_ld16(T0 + TM_D + lane_base + D + 64 * hf + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        st_stream_f4(aw + c + j, make_float4(tc::to_tf32(-v[j]), tc::to_tf32(-v[j + 1]),
-                                                             tc::to_tf32(-v[j + 2]), tc::to_tf32(-v[j + 3])));
+                    for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(-v[j]);
+                    st_stream_f8(aw + c, v);
+                    st_stream_f8(aw + c + 8, v + 8);
                 }
             } else {
                 const int t = row - C;
@@ -636,8 +637,8 @@ prep_kernel(kda_prefill_args a, Work w,
                         const int d = 64 * hf + c + j;
                         o4[j] = tc::to_tf32(sQ[t * QS + d] * es[d] - v[j]);
                     }
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) st_stream_f4(aw + c + j, make_float4(o4[j], o4[j + 1], o4[j + 2], o4[j + 3]));
+                    st_stream_f8(aw + c, o4);
+                    st_stream_f8(aw + c + 8, o4 + 8);
                 }
             }
             tc::fence_before_sync();
@@ -655,59 +656,88 @@ prep_kernel(kda_prefill_args a, Work w,
 // ---------------------------------------------------------------------------
 // scan: the state recurrence over one sequence's records
 // ---------------------------------------------------------------------------
-namespace scan {
-constexpr int AW_TILE = 128 * 128 * 4;              // SW128 [128 rows][128 K]
-constexpr int OFF_AW0 = 0;
-constexpr int OFF_AW1 = AW_TILE;
-constexpr int OFF_SOP = 2 * AW_TILE;                // S operand, SW128 [e][d]        32 KB
-constexpr int OFF_VOP = OFF_SOP + NE * D * 4;       // V' operand, SW128 [e][t]       16 KB
-constexpr int OFF_G0 = OFF_VOP + NE * C * 4;        // g_in tiles, [C][64] bf16 swizzled
-constexpr int OFF_G1 = OFF_G0 + C * NE * 2;
-constexpr int OFF_SMALL = OFF_G1 + C * NE * 2;
-constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * C, SM_FLOATS = 4 * C;
-constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
-static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0 && OFF_G1 % 1024 == 0,
-              "swizzled tiles need 1024-B alignment");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-constexpr uint32_t TM_D = 0;      // 2 x 64 cols: [U ; U_o] -> [V' ; O], by chunk parity
-constexpr uint32_t TM_A3 = 128;   // 2 x 64 cols: (K gamma_C / Gamma)^T, by chunk parity
-constexpr uint32_t TM_DS = 256;   // 64 cols: state increment
-constexpr uint32_t TM_S = 320;    // 64 cols: FP32 state
-constexpr uint32_t TM_COLS = 512;
-}  // namespace scan
+// scan shared-memory / TMEM layout for a cluster of R CTAs per (sequence, head),
+// each owning NE = 128 / R value columns
+template <int R>
+struct ScanCfg {
+    static constexpr int NE = D / R;
+    static constexpr int AW_TILE = 128 * 128 * 4;            // SW128 [128 rows][128 K]
+    static constexpr int OFF_AW0 = 0;
+    static constexpr int OFF_AW1 = AW_TILE;
+    static constexpr int OFF_SOP = 2 * AW_TILE;              // S operand, SW128 [e][d]
+    static constexpr int OFF_VOP = OFF_SOP + NE * D * 4;     // V' operand, SW128 [e][t]
+    static constexpr int G_TILE = C * NE * 2;                // g_in tile, [C][NE] bf16
+    static constexpr int OFF_G0 = OFF_VOP + NE * C * 4;
+    static constexpr int OFF_G1 = OFF_G0 + G_TILE;
+    static constexpr int OFF_SMALL = OFF_G1 + G_TILE;
+    // small region (floats): peers' row sums [2 parity][R source][C], own halves [2][2][C]
+    static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_FLOATS = SM_ROWPART + 4 * C;
+    static constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
+    static constexpr uint32_t TM_D = 0;                      // 2 x NE cols: [U ; U_o] -> [V' ; O]
+    static constexpr uint32_t TM_A3 = 2 * NE;                // 2 x 64 cols: (K gamma_C / Gamma)^T
+    static constexpr uint32_t TM_DS = TM_A3 + 2 * C;         // NE cols: state increment
+    static constexpr uint32_t TM_S = TM_DS + NE;             // NE cols: FP32 state
+    static constexpr uint32_t TM_COLS = (TM_S + NE) <= 256 ? 256 : 512;
+    static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0, "1024-B aligned operands");
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(TM_S + NE <= TM_COLS, "TMEM budget");
+};
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
+TC_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+TC_DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
+TC_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// byte offset of bf16 element (row, col) in a g_in tile of NE columns: the 128-byte
+// rows of NE = 64 come swizzled by TMA, narrower rows are plain
+template <int NE>
+TC_DEV uint32_t gtile_offset(int row, int col) {
+    if constexpr (NE == 64) return sw128_bf16(row, col);
+    else return (uint32_t)(row * NE * 2 + col * 2);
+}
+
+// Per chunk, the recurrence path is MMA 2 -> V' operand -> MMA 3 -> state update.
+// The chunk's output rows take no part in it: the epilogue of chunk j only forms
+// their sums of squares, and o, y of chunk j are written during chunk j+1's
+// MMA 2 from the TMEM buffer that still holds them.  The R CTAs' row sums meet
+// through distributed shared memory behind a split cluster barrier (arrive in
+// chunk j, wait in chunk j+1), so no CTA stalls on its peers.
+template <int R>
+__global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(NT, 1)
 scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
             const __grid_constant__ CUtensorMap tm_g) {
-    using namespace scan;
+    using Cfg = ScanCfg<R>;
+    constexpr int NE = Cfg::NE;
+    constexpr int HW = NE / 2;           // value columns per thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sSop = sm + OFF_SOP;
-    uint8_t* sVop = sm + OFF_VOP;
-    float* fs = reinterpret_cast<float*>(sm + OFF_SMALL);
-    float* s_rowsq = fs + SM_ROWSQ;      // [2][C] peer's row sums of squares (by chunk parity)
-    float* s_rowpart = fs + SM_ROWPART;  // [2][C] this CTA's, per column half
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
+    uint8_t* sSop = sm + Cfg::OFF_SOP;
+    uint8_t* sVop = sm + Cfg::OFF_VOP;
+    float* fs = reinterpret_cast<float*>(sm + Cfg::OFF_SMALL);
+    float* s_rowsq = fs + Cfg::SM_ROWSQ;      // [2][R][C] peers' row sums, by parity and source
+    float* s_rowpart = fs + Cfg::SM_ROWPART;  // [2][2][C] this CTA's, by parity and column half
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + Cfg::SM_FLOATS);
     uint64_t* bar_aw = mbar + 1;         // [2]
     uint64_t* bar_g = mbar + 3;          // [2]
     uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 5);
 
-    const int r = blockIdx.x;
+    const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
     const int n = blockIdx.z;
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, hf = warp >> 2;
     const int row = quad * 32 + lane;
-    const int c_lo = hf * (NE / 2);
+    const int c_lo = hf * HW;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
     const int g0 = w.chunk_base[n];
     const int nch = w.chunk_base[n + 1] - g0;
     const bool gate = a.g_in != nullptr;
     auto rec_of = [&](int j) { return (long)(g0 + j) * H + h; };
+    auto aw_buf = [&](int b) { return sm + (b ? Cfg::OFF_AW1 : Cfg::OFF_AW0); };
+    auto g_buf = [&](int b) { return sm + (b ? Cfg::OFF_G1 : Cfg::OFF_G0); };
 
-    if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
+    if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
         for (int b = 0; b < 2; ++b) { tc::mbar_init(bar_aw + b, 1); tc::mbar_init(bar_g + b, 1); }
@@ -715,13 +745,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         tc::tma_prefetch_desc(&tm_aw);
         if (gate) tc::tma_prefetch_desc(&tm_g);
         for (int j = 0; j < 2 && j < nch; ++j) {
-            uint8_t* dst = sm + (j ? OFF_AW1 : OFF_AW0);
-            tc::mbar_arrive_expect_tx(bar_aw + j, AW_TILE);
+            tc::mbar_arrive_expect_tx(bar_aw + j, Cfg::AW_TILE);
             for (int s = 0; s < 4; ++s)
-                tc::tma_load_2d(dst + s * (AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + j);
+                tc::tma_load_2d(aw_buf(j) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + j);
             if (gate) {
-                tc::mbar_arrive_expect_tx(bar_g + j, C * NE * 2);
-                tc::tma_load_2d(sm + (j ? OFF_G1 : OFF_G0), &tm_g, h * D + NE * r, t_begin + C * j, bar_g + j);
+                tc::mbar_arrive_expect_tx(bar_g + j, Cfg::G_TILE);
+                tc::tma_load_2d(g_buf(j), &tm_g, h * D + NE * r, t_begin + C * j, bar_g + j);
             }
         }
     }
@@ -732,7 +761,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint32_t ph_mma = 0;
     bool timed_out = false;
     // a wait that gives up records it, and every later wait is skipped (the loop
-    // keeps its cluster barriers, so the peer CTA is never left waiting)
+    // keeps its cluster barriers, so the peer CTAs are never left waiting)
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
     };
@@ -742,38 +771,86 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         tc::fence_after_sync();
     };
 
-    // record loads into registers: [U ; U_o] row `row`, this CTA's 32 columns of
-    // this thread; (K gamma_C / Gamma)^T row `row`, tokens c_lo..c_lo+31
-    float4 pu[8], pk[8];
+    // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
+    // CTA's columns; (K gamma_C / Gamma)^T row `row`, tokens 32*hf..32*hf+31; gamma_C[row]
+    float pu[HW], pk[32], pg = 0.f;
     auto load_rec = [&](int j) {
         const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
-        const float* k = w.kt + rec_of(j) * KT_FLOATS + (size_t)row * C + c_lo;
+        const float* k = w.kt + rec_of(j) * KT_FLOATS + (size_t)row * C + 32 * hf;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { pu[i] = ld_f4(u + 4 * i); pk[i] = ld_f4(k + 4 * i); }
+        for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_nc_f8(k + 8 * i, pk + 8 * i);
+        pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
     };
     auto store_rec = [&](int b) {
 #pragma unroll
-        for (int i = 0; i < 8; i += 4) {
-            tc::tmem_st16(T0 + TM_D + 64 * b + lane_base + c_lo + 4 * i, reinterpret_cast<const float*>(pu + i));
-            tc::tmem_st16(T0 + TM_A3 + 64 * b + lane_base + c_lo + 4 * i, reinterpret_cast<const float*>(pk + i));
+        for (int i = 0; i < HW; i += 16)
+            tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
+#pragma unroll
+        for (int i = 0; i < 32; i += 16)
+            tc::tmem_st16(T0 + Cfg::TM_A3 + C * b + lane_base + 32 * hf + i, pk + i);
+    };
+    // o and y of chunk jo from its TMEM buffer (output-row threads, row >= C)
+    auto emit_outputs = [&](int jo) {
+        const int bo = jo & 1;
+        const int t = row - C;
+        const int c0o = t_begin + C * jo;
+        const int nco = min(C, t_end - c0o);
+        float o[HW];
+#pragma unroll
+        for (int c = 0; c < HW; c += 16) tc::tmem_ld16(T0 + Cfg::TM_D + NE * bo + lane_base + c_lo + c, o + c);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < HW; ++c) o[c] *= a.scale;
+        if (t < nco) {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+            for (int c = 0; c < HW; c += 8) store8_bf16(dst + c, o + c);
+        }
+        if (gate) {
+            wait(bar_g + bo, (jo >> 1) & 1);
+            if (t < nco) {
+                const uint8_t* sG = g_buf(bo);
+                float tot = s_rowpart[(bo * 2) * C + t] + s_rowpart[(bo * 2 + 1) * C + t];
+#pragma unroll
+                for (int p = 0; p < R; ++p)
+                    if (p != r) tot += s_rowsq[(bo * R + p) * C + t];
+                const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
+                uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+                for (int c = 0; c < HW; c += 8) {
+                    const uint4 g8 = *reinterpret_cast<const uint4*>(sG + gtile_offset<NE>(t, c_lo + c));
+                    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                    float yv[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
+                        const float wn = a.norm_w ? a.norm_w[NE * r + c_lo + c + jj] : 1.f;
+                        yv[jj] = sigmoidf_fast(gv) * wn * o[c + jj] * rr;
+                    }
+                    store8_bf16(yp + c, yv);
+                }
+            }
         }
     };
 
     // ---- initial state -> TMEM master copy and the tf32 operand copy
+    float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
     {
         const int d = row;
         const size_t sb = (((size_t)n * H + h) * D + d) * D + NE * r;
         float v[16];
 #pragma unroll
-        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
+        for (int c = c_lo; c < c_lo + HW; c += 16) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = a.S0 ? a.S0[sb + c + j] : 0.f;
-            tc::tmem_st16(T0 + TM_S + lane_base + c, v);
+            for (int jj = 0; jj < 16; ++jj) v[jj] = a.S0 ? a.S0[sb + c + jj] : 0.f;
+            tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, v);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + j, d, NE)) = tc::to_tf32(v[j]);
+            for (int jj = 0; jj < 16; ++jj)
+                *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(v[jj]);
         }
-        if (nch > 0) { load_rec(0); store_rec(0); }
+        if (nch > 0) { load_rec(0); store_rec(0); gm_next = pg; }
         if (nch > 1) load_rec(1);
         tc::tmem_st_wait();
         tc::fence_proxy_async();
@@ -786,64 +863,60 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         const int b = j & 1;
         const int c0 = t_begin + C * j;
         const int nc = min(C, t_end - c0);
-        const long rec = rec_of(j);
-        const float gm = w.gm[rec * GM_FLOATS + row];
+        const float gm = gm_next;
 
         // ---- MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S
         if (tid == 0) {
             wait(bar_aw + b, (j >> 1) & 1);
             tc::fence_after_sync();
-            const uint32_t ab = tc::smem_u32(sm + (b ? OFF_AW1 : OFF_AW0));
+            const uint32_t ab = tc::smem_u32(aw_buf(b));
             const uint32_t sb = tc::smem_u32(sSop);
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ss(T0 + TM_D + 64 * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
+                tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
                                 tc::idesc_tf32(128, NE), 1);
             tc::mma_commit(mbar);
         }
-        // the next record's [U ; U_o] and (K gamma_C/Gamma)^T into the other TMEM buffers,
-        // then fetch the one after it
-        if (j + 1 < nch) store_rec(b ^ 1);
+        // while it runs: outputs of the previous chunk (their buffer is refilled next),
+        // the next record into the other TMEM buffers, the one after it into registers
+        if (j > 0) {
+            if (gate) cluster_wait();
+            if (row >= C) emit_outputs(j - 1);
+        }
+        if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
         if (j + 2 < nch) load_rec(j + 2);
         tc::tmem_st_wait();
         mma_wait();
         if (tid == 0 && j + 2 < nch) {   // the A tile of this chunk is consumed
-            tc::mbar_arrive_expect_tx(bar_aw + b, AW_TILE);
+            tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
             for (int s = 0; s < 4; ++s)
-                tc::tma_load_2d(sm + (b ? OFF_AW1 : OFF_AW0) + s * (AW_TILE / 4), &tm_aw, 32 * s,
-                                (int)(rec_of(j + 2) * 128), bar_aw + b);
+                tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
         }
 
-        // ---- V' -> operand (smem), O -> o, row sums of squares for the output gate
-        float o[NE / 2];
+        // ---- V' -> operand (smem); output rows: sums of squares for the gate
         {
             float v[16];
-            float ss = 0.f;
             if (row < C) {
                 const int t = row;
 #pragma unroll
-                for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + 64 * b + lane_base + c, v);
+                for (int c = c_lo; c < c_lo + HW; c += 16) {
+                    tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + jj, t, C)) = tc::to_tf32(v[jj]);
+                        *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + jj, t, NE)) = tc::to_tf32(v[jj]);
                 }
-            } else {
+            } else if (gate) {
                 const int t = row - C;
+                float ss = 0.f;
 #pragma unroll
-                for (int c = 0; c < NE / 2; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + 64 * b + lane_base + c_lo + c, v);
+                for (int c = c_lo; c < c_lo + HW; c += 16) {
+                    tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) { o[c + jj] = a.scale * v[jj]; ss += o[c + jj] * o[c + jj]; }
+                    for (int jj = 0; jj < 16; ++jj) ss = fmaf(v[jj], v[jj], ss);
                 }
-                if (t < nc) {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
-#pragma unroll
-                    for (int c = 0; c < NE / 2; c += 8) store8_bf16(dst + c, o + c);
-                }
-                if (gate) s_rowpart[hf * C + t] = ss;
+                s_rowpart[(b * 2 + hf) * C + t] = ss * a.scale * a.scale;
             }
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -856,41 +929,26 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             const uint32_t vb = tc::smem_u32(sVop);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(T0 + TM_DS, T0 + TM_A3 + 64 * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
+                tc::mma_tf32_ts(T0 + Cfg::TM_DS, T0 + Cfg::TM_A3 + C * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
                                 tc::idesc_tf32(128, NE), ks > 0);
             tc::mma_commit(mbar);
-        }
-
-        // ---- fused output gate (row RMS over both CTAs' columns), while MMA 3 runs
-        if (gate) {
-            const int par = j & 1;
-            if (row >= C && hf == 0) {
-                const int t = row - C;
-                st_cluster_f32(cluster_map(s_rowsq + par * C + t, r ^ 1), s_rowpart[t] + s_rowpart[C + t]);
+            // the g_in tile of chunk j-1 is consumed (its outputs were emitted above)
+            if (gate && j >= 1 && j + 1 < nch) {
+                tc::mbar_arrive_expect_tx(bar_g + (b ^ 1), Cfg::G_TILE);
+                tc::tma_load_2d(g_buf(b ^ 1), &tm_g, h * D + NE * r, t_begin + C * (j + 1), bar_g + (b ^ 1));
             }
-            cluster_sync_all();
-            if (row >= C) {
+        }
+        if (gate) {   // this chunk's row sums to every peer, then arrive (waited on next chunk)
+            const bool writer = row >= C && hf == 0;
+            if (writer) {
                 const int t = row - C;
-                wait(bar_g + b, (j >> 1) & 1);
-                if (t < nc) {
-                    const uint8_t* sG = sm + (b ? OFF_G1 : OFF_G0);
-                    const float tot = s_rowpart[t] + s_rowpart[C + t] + s_rowsq[par * C + t];
-                    const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                    uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
+                const float own = s_rowpart[(b * 2) * C + t] + s_rowpart[(b * 2 + 1) * C + t];
 #pragma unroll
-                    for (int c = 0; c < NE / 2; c += 8) {
-                        const uint4 g8 = *reinterpret_cast<const uint4*>(sG + sw128_bf16(t, c_lo + c));
-                        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
-                        float yv[8];
-#pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
-                            const float wn = a.norm_w ? a.norm_w[NE * r + c_lo + c + jj] : 1.f;
-                            yv[jj] = sigmoidf_fast(gv) * wn * o[c + jj] * rr;
-                        }
-                        store8_bf16(yp + c, yv);
-                    }
-                }
+                for (int p = 1; p < R; ++p)
+                    st_cluster_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own);
+                cluster_arrive();
+            } else {
+                cluster_arrive_relaxed();
             }
         }
 
@@ -907,13 +965,13 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             }
             float dv[16], sv[16];
 #pragma unroll
-            for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
-                tc::tmem_ld16(T0 + TM_DS + lane_base + c, dv);
-                tc::tmem_ld16(T0 + TM_S + lane_base + c, sv);
+            for (int c = c_lo; c < c_lo + HW; c += 16) {
+                tc::tmem_ld16(T0 + Cfg::TM_DS + lane_base + c, dv);
+                tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, sv);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
-                tc::tmem_st16(T0 + TM_S + lane_base + c, sv);
+                tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, sv);
                 if (snap) {
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4)
@@ -928,12 +986,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             tc::fence_before_sync();
         }
         __syncthreads();
-        // the g_in tile of this chunk is consumed: fetch the one two chunks ahead
-        if (tid == 0 && gate && j + 2 < nch) {
-            tc::fence_proxy_async();
-            tc::mbar_arrive_expect_tx(bar_g + b, C * NE * 2);
-            tc::tma_load_2d(sm + (b ? OFF_G1 : OFF_G0), &tm_g, h * D + NE * r, t_begin + C * (j + 2), bar_g + b);
-        }
+    }
+    // outputs of the last chunk
+    if (nch > 0) {
+        if (gate) cluster_wait();
+        if (row >= C) emit_outputs(nch - 1);
     }
 
     // ---- final state
@@ -942,8 +999,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         float* dst = a.S_T + (((size_t)n * H + h) * D + d) * D + NE * r;
         float v[16];
 #pragma unroll
-        for (int c = c_lo; c < c_lo + NE / 2; c += 16) {
-            tc::tmem_ld16(T0 + TM_S + lane_base + c, v);
+        for (int c = c_lo; c < c_lo + HW; c += 16) {
+            tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, v);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int jj = 0; jj < 16; jj += 4)
@@ -954,8 +1011,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     drain_if(timed_out);
     tc::fence_before_sync();
     __syncthreads();
-    cluster_sync_all();   // no CTA leaves while its peer may still write to its shared memory
-    if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
+    cluster_sync_all();   // no CTA leaves while a peer may still write to its shared memory
+    if (warp == 0) tc::tmem_dealloc(T0, Cfg::TM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -969,16 +1026,19 @@ static long total_chunks(const kda_prefill_args& a) {
     return c;
 }
 
-struct Layout { size_t base, aw, uu, kt, gm, total; long nrec; };
+// workspace: error word at 0, chunk offsets at 256, then the record arrays from
+// the first 1024-byte aligned address after them (the size allows for the slack)
+struct Layout { size_t base, rec_start, aw, uu, kt, gm, total; long nrec; };
 static Layout layout(const kda_prefill_args& a) {
     Layout l;
     l.nrec = total_chunks(a) * a.H;
-    l.base = 256;                                            // error word first
-    l.aw = align_up(l.base + 4 * (size_t)(a.num_seqs + 1), 1024);
+    l.base = 256;
+    l.rec_start = l.base + 4 * (size_t)(a.num_seqs + 1);
+    l.aw = 0;                                               // relative to the aligned record start
     l.uu = l.aw + (size_t)l.nrec * AW_FLOATS * 4;
     l.kt = l.uu + (size_t)l.nrec * UU_FLOATS * 4;
     l.gm = l.kt + (size_t)l.nrec * KT_FLOATS * 4;
-    l.total = l.gm + (size_t)l.nrec * GM_FLOATS * 4;
+    l.total = l.rec_start + 1024 + l.gm + (size_t)l.nrec * GM_FLOATS * 4;
     return l;
 }
 
@@ -1003,8 +1063,8 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
         attr_err = cudaFuncSetAttribute(spl::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         spl::prep::SMEM_BYTES);
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(spl::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            spl::scan::SMEM_BYTES);
+            attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (a.num_seqs == 0) return cudaSuccess;
@@ -1013,10 +1073,11 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
     spl::Work w;
     w.err = reinterpret_cast<int*>(ws);
     w.chunk_base = reinterpret_cast<const int*>(ws + L.base);
-    w.aw = reinterpret_cast<float*>(ws + L.aw);
-    w.uu = reinterpret_cast<float*>(ws + L.uu);
-    w.kt = reinterpret_cast<float*>(ws + L.kt);
-    w.gm = reinterpret_cast<float*>(ws + L.gm);
+    uint8_t* recs = reinterpret_cast<uint8_t*>(spl::align_up(reinterpret_cast<uintptr_t>(ws) + L.rec_start, 1024));
+    w.aw = reinterpret_cast<float*>(recs + L.aw);
+    w.uu = reinterpret_cast<float*>(recs + L.uu);
+    w.kt = reinterpret_cast<float*>(recs + L.kt);
+    w.gm = reinterpret_cast<float*>(recs + L.gm);
     w.nrec = L.nrec;
 
     const uint64_t rowq = (uint64_t)a.H * spl::D;
@@ -1031,8 +1092,9 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
                       CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
     if ((e = make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, rowq, rows, 64, spl::C,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-    if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, rowq, rows, spl::NE,
-                      spl::C, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    constexpr int NE = spl::ScanCfg<spl::SCAN_R>::NE;
+    if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, rowq, rows, NE, spl::C,
+                      NE == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
     if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.aw, 128, (uint64_t)L.nrec * 128, 32, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
 
@@ -1044,8 +1106,8 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
         spl::prep_kernel<<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
         ++launched;
     }
-    dim3 grid(2, a.H, a.num_seqs);
-    spl::scan_kernel<<<grid, spl::NT, spl::scan::SMEM_BYTES, s>>>(a, w, maw, mg);
+    dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
+    spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg);
     ++launched;
     count_launches(launched);
     return cudaGetLastError();
