@@ -180,9 +180,9 @@ def nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
-def kernel_traffic(kernel_file, name):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source
-    still matches the hash recorded with it (else None)."""
+def kernel_traffic(kernel_file, name, field="bytes_per_launch"):
+    """A field of the committed ncu summary (DRAM bytes per launch by default),
+    if the kernel source still matches the hash recorded with it (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -190,7 +190,7 @@ def kernel_traffic(kernel_file, name):
         rec = json.load(open(p)).get(name)
         src = open(os.path.join(ROOT, "serving_kda_chunked_gated_gb300", "csrc", kernel_file), "rb").read()
         if rec and rec.get("source_sha256") == hashlib.sha256(src).hexdigest():
-            return rec.get("bytes_per_launch")
+            return rec.get(field)
     except (OSError, ValueError):
         pass
     return None
@@ -360,9 +360,11 @@ def run_ours(args, rank, world):
                    "qkv": "bf16", "S0": wl["S0"], "fused_gate": wl["gate"], "qk_l2norm": True,
                    "l2": "inputs larger than L2 (no flush needed)", "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm"], "traffic": kernel_traffic("prefill_tc.cu", "prefill"),
+                     "frac": achieved / pk["hbm"], "traffic": kernel_traffic("prefill_split.cu", "prefill"),
                      "peak_source": pk["src"] + " hbm_gbs (burst copy)",
+                     "launch": "one kda_prefill call: plan + prep (all chunks in parallel) + scan (state recurrence)",
                      "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernels": kernel_traffic("prefill_split.cu", "prefill", "kernels"),
                      "tensor": {"achieved_tflops": alg_flops / (ms * 1e-3) / 1e12,
                                 "peak_tf32_tflops": tf32_peak,
                                 "frac_of_tf32": alg_flops / (ms * 1e-3) / 1e12 / tf32_peak,
