@@ -348,10 +348,12 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
 
-        // ---- 2. Gram sub-blocks, mma.sync tf32: blocks 0..9 of A_qk, 10..19 of A_kk;
-        //         warp w owns blocks w, w+8, w+16
+        // ---- 2. Gram sub-blocks, mma.sync tf32: blocks 0..9 of A_qk, 10..19 of A_kk.
+        //         Warp w forms blocks w and w+8 whole and one K-half (w & 1) of block
+        //         16 + w/2; the two halves of blocks 16..19 are added in a fixed order.
         {
             const int g = lane >> 2, t4 = lane & 3;
+            float* part = sAkk + C * AS;               // [8 warps][16][16] half-block partials
             float acc[3][2][4];
 #pragma unroll
             for (int it = 0; it < 3; ++it)
@@ -360,23 +362,23 @@ prep_kernel(kda_prefill_args a, Work w,
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
             int ia[3], ib[3];
-            bool kk[3], on[3];
+            bool kk[3];
 #pragma unroll
             for (int it = 0; it < 3; ++it) {
-                const int blk_id = warp + 8 * it;
-                on[it] = blk_id < 2 * NPAIR;
+                const int blk_id = it < 2 ? warp + 8 * it : 16 + (warp >> 1);
                 kk[it] = blk_id >= NPAIR;
                 const int pr = kk[it] ? blk_id - NPAIR : blk_id;
                 const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
                 ia[it] = aa;
                 ib[it] = pr - aa * (aa + 1) / 2;
             }
+            const int khalf = warp & 1;
 #pragma unroll 2
             for (int ks = 0; ks < 16; ++ks) {
                 const int k0 = 8 * ks + t4, k1 = k0 + 4;
 #pragma unroll
                 for (int it = 0; it < 3; ++it) {
-                    if (on[it]) {
+                    if (it < 2 || (ks >> 3) == khalf) {
                         const float* Arows = kk[it] ? sKr : sQ;
                         const int ra = 16 * ia[it] + g;
                         const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
@@ -394,25 +396,42 @@ prep_kernel(kda_prefill_args a, Work w,
             }
 #pragma unroll
             for (int it = 0; it < 3; ++it) {
-                if (on[it]) {
-                    float* Out = kk[it] ? sAkk : sAqk;
+                float* Out = kk[it] ? sAkk : sAqk;
 #pragma unroll
-                    for (int nh = 0; nh < 2; ++nh) {
+                for (int nh = 0; nh < 2; ++nh) {
 #pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const int I = 16 * ia[it] + g + 8 * hr;
-                            const int J = 16 * ib[it] + 8 * nh + 2 * t4;
-                            float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
-                            if (!kk[it]) { if (J > I) v0 = 0.f; if (J + 1 > I) v1 = 0.f; }
-                            else {
-                                const float bI = s_beta[I];
-                                v0 = (J >= I) ? 0.f : v0 * bI;
-                                v1 = (J + 1 >= I) ? 0.f : v1 * bI;
-                            }
-                            *reinterpret_cast<float2*>(Out + I * AS + J) = make_float2(v0, v1);
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int I = 16 * ia[it] + g + 8 * hr;
+                        const int J = 16 * ib[it] + 8 * nh + 2 * t4;
+                        float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
+                        if (it == 2) {   // raw half-block partial
+                            *reinterpret_cast<float2*>(part + warp * 256 + (g + 8 * hr) * 16 + 8 * nh + 2 * t4) =
+                                make_float2(v0, v1);
+                            continue;
                         }
+                        if (!kk[it]) { if (J > I) v0 = 0.f; if (J + 1 > I) v1 = 0.f; }
+                        else {
+                            const float bI = s_beta[I];
+                            v0 = (J >= I) ? 0.f : v0 * bI;
+                            v1 = (J + 1 >= I) ? 0.f : v1 * bI;
+                        }
+                        *reinterpret_cast<float2*>(Out + I * AS + J) = make_float2(v0, v1);
                     }
                 }
+            }
+            __syncthreads();
+            {   // blocks 16..19 = A_kk pairs (3, q), q = 0..3: halves from warps 2q and 2q+1
+                const int q = tid >> 6, e = (tid & 63) * 4;
+                const int I = 48 + (e >> 4), J = 16 * q + (e & 15);
+                const float4 h0 = *reinterpret_cast<const float4*>(part + (2 * q) * 256 + e);
+                const float4 h1 = *reinterpret_cast<const float4*>(part + (2 * q + 1) * 256 + e);
+                const float bI = s_beta[I];
+                float4 o;
+                o.x = (J >= I) ? 0.f : (h0.x + h1.x) * bI;
+                o.y = (J + 1 >= I) ? 0.f : (h0.y + h1.y) * bI;
+                o.z = (J + 2 >= I) ? 0.f : (h0.z + h1.z) * bI;
+                o.w = (J + 3 >= I) ? 0.f : (h0.w + h1.w) * bI;
+                *reinterpret_cast<float4*>(sAkk + I * AS + J) = o;
             }
         }
         __syncthreads();
@@ -633,9 +652,14 @@ prep_kernel(kda_prefill_args a, Work w,
                     tc::tmem_ld_wait();
                     float o4[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 16; j += 4) {
                         const int d = 64 * hf + c + j;
-                        o4[j] = tc::to_tf32(sQ[t * QS + d] * es[d] - v[j]);
+                        const float4 q4 = *reinterpret_cast<const float4*>(sQ + t * QS + d);
+                        const float4 e4 = *reinterpret_cast<const float4*>(es + d);
+                        o4[j] = tc::to_tf32(q4.x * e4.x - v[j]);
+                        o4[j + 1] = tc::to_tf32(q4.y * e4.y - v[j + 1]);
+                        o4[j + 2] = tc::to_tf32(q4.z * e4.z - v[j + 2]);
+                        o4[j + 3] = tc::to_tf32(q4.w * e4.w - v[j + 3]);
                     }
                     st_stream_f8(aw + c, o4);
                     st_stream_f8(aw + c + 8, o4 + 8);
