@@ -64,9 +64,11 @@ def _load():
         lib.kda_oracle_prefill.argtypes = [
             ctypes.c_int, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int, ctypes.c_int,
             d, d, d, d, d, d, ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_double,
-            d, d, d, d, d, ctypes.c_double, d, ctypes.c_int, d]
+            d, d, d, d, d, ctypes.c_double, d, ctypes.c_int, d, ctypes.c_int]
         lib.kda_oracle_log_decay.restype = ctypes.c_double
         lib.kda_oracle_log_decay.argtypes = [ctypes.c_double] * 3
+        lib.kda_oracle_log_decay_softplus.restype = ctypes.c_double
+        lib.kda_oracle_log_decay_softplus.argtypes = [ctypes.c_double] * 2
         lib.kda_oracle_gate_norm.restype = None
         lib.kda_oracle_gate_norm.argtypes = [d, d, d, ctypes.c_double, d, ctypes.c_long, ctypes.c_int]
         lib.kda_oracle_num_threads.restype = ctypes.c_int
@@ -90,20 +92,27 @@ def num_threads() -> int:
     return int(_load().kda_oracle_num_threads())
 
 
-def log_decay(z, A_h: float, g_min: float = G_MIN) -> np.ndarray:
-    """Bounded decay gate, Sec. 2.2: g = g_min * Sigmoid(exp(A_h) z), elementwise."""
+GATES = {"bounded": 0, "softplus": 1}
+
+
+def log_decay(z, A_h: float, g_min: float = G_MIN, gate: str = "bounded") -> np.ndarray:
+    """Decay gate of Sec. 2.2, elementwise: K3's bounded g = g_min * Sigmoid(exp(A_h) z)
+    (gate="bounded"), or Kimi Linear's g = -exp(A_h) * Softplus(z) (gate="softplus")."""
     lib = _load()
     z = np.asarray(z, dtype=np.float64)
     out = np.empty_like(z)
     flat, of = z.reshape(-1), out.reshape(-1)
     for i in range(flat.size):
-        of[i] = lib.kda_oracle_log_decay(float(flat[i]), float(A_h), float(g_min))
+        if GATES[gate]:
+            of[i] = lib.kda_oracle_log_decay_softplus(float(flat[i]), float(A_h))
+        else:
+            of[i] = lib.kda_oracle_log_decay(float(flat[i]), float(A_h), float(g_min))
     return out
 
 
 def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
             g_min=G_MIN, scale=1.0, qk_l2norm=True, l2_eps=L2_EPS, norm_eps=NORM_EPS,
-            want_state=True, snap_interval=0):
+            want_state=True, snap_interval=0, gate="bounded"):
     """Per-token recurrence, Sec. 2.1, over packed sequences.
 
     q, k, z: [tok, H, dk]; v: [tok, H, dv]; beta: [tok, H]; A: [H];
@@ -111,7 +120,8 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
     Returns (o [tok,H,dv], S_T [N,H,dk,dv] or None, y [tok,H,dv] or None), FP64,
     and, when snap_interval > 0, the prefix-cache snapshots [rows, H, dk, dv]:
     the state of each sequence after every snap_interval of its tokens, the
-    sequences' rows in order (Sec. 13.1 prefix cache).
+    sequences' rows in order (Sec. 13.1 prefix cache).  gate: "bounded" (K3) or
+    "softplus" (Kimi Linear), see log_decay.
     """
     lib = _load()
     q, k, v, z, beta, A = map(_f64, (q, k, v, z, beta, A))
@@ -136,14 +146,15 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
         _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A),
         float(g_min), float(scale), int(bool(qk_l2norm)), float(l2_eps),
         _ptr(S0), _ptr(o), _ptr(S_T), _ptr(g_in), _ptr(norm_w), float(norm_eps), _ptr(y),
-        int(snap_interval), _ptr(S_snap) if S_snap is not None and S_snap.size else None)
+        int(snap_interval), _ptr(S_snap) if S_snap is not None and S_snap.size else None, GATES[gate])
     if snap_interval:
         return o, S_T, y, S_snap
     return o, S_T, y
 
 
 def decode_step(q, k, v, z, beta, A, state, slots=None, g_in=None, norm_w=None,
-                g_min=G_MIN, scale=1.0, qk_l2norm=True, l2_eps=L2_EPS, norm_eps=NORM_EPS):
+                g_min=G_MIN, scale=1.0, qk_l2norm=True, l2_eps=L2_EPS, norm_eps=NORM_EPS,
+                gate="bounded"):
     """One recurrent step per sequence (Sec. 2.1 with one token each).
 
     q, k, z: [N, H, dk]; v: [N, H, dv]; state: [S, H, dk, dv] (not modified);
@@ -156,7 +167,7 @@ def decode_step(q, k, v, z, beta, A, state, slots=None, g_in=None, norm_w=None,
     cu = np.arange(N + 1, dtype=np.int32)
     o, S_T, y = prefill(q, k, v, z, beta, A, cu_seqlens=cu, S0=state[slots], g_in=g_in,
                         norm_w=norm_w, g_min=g_min, scale=scale, qk_l2norm=qk_l2norm,
-                        l2_eps=l2_eps, norm_eps=norm_eps)
+                        l2_eps=l2_eps, norm_eps=norm_eps, gate=gate)
     new_state = state.copy()
     new_state[slots] = S_T
     return o, new_state, y

@@ -13,7 +13,9 @@
  *       o~_t = S_t^T q_t
  *     with q, k passed through L2Norm and beta_t in (0, 1).
  *   Sec. 2.2, bounded decay gate:
- *       g_t = g_min * Sigmoid(exp(A_h) * z_t),  alpha_t = exp(g_t),  g_min = -5.
+ *       g_t = g_min * Sigmoid(exp(A_h) * z_t),  alpha_t = exp(g_t),  g_min = -5,
+ *     and, with gate_mode = 1, the gate it replaces (Kimi Linear's, printed beside
+ *     it in Sec. 2.2):  g_t = -exp(A_h) * Softplus(z_t), unbounded below.
  *   Sec. 2.3, full-rank output gate (the W_o projection and the W_g x
  *   product are outside this operator; g_in = W_g x is an input):
  *       y_t = Sigmoid(g_in_t) (.) RMSNorm(o~_t).
@@ -53,6 +55,13 @@ static void l2normalise(const double* x, double* out, int n, double eps) {
 }
 
 /* The decay gate of Sec. 2.2 for one channel: log-retention g. */
+/* Softplus(x) = log(1 + e^x), written so that neither branch overflows */
+static double softplus(double x) { return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x))); }
+
+/* Kimi Linear's gate (Sec. 2.2, the mapping K3 replaces): g = -exp(A_h) Softplus(z),
+ * unbounded below */
+double kda_oracle_log_decay_softplus(double z, double A_h) { return -exp(A_h) * softplus(z); }
+
 double kda_oracle_log_decay(double z, double A_h, double g_min) {
     return g_min * sigmoid(exp(A_h) * z);
 }
@@ -84,7 +93,7 @@ void kda_oracle_prefill(int num_seqs, const int32_t* cu_seqlens, int H, int dk, 
                         double g_min, double scale, int qk_l2norm, double l2_eps,
                         const double* S0, double* o, double* S_T,
                         const double* g_in, const double* norm_w, double norm_eps,
-                        double* y, int snap_interval, double* S_snap) {
+                        double* y, int snap_interval, double* S_snap, int gate_mode) {
     long pairs = (long)num_seqs * H;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)
@@ -114,7 +123,7 @@ void kda_oracle_prefill(int num_seqs, const int32_t* cu_seqlens, int H, int dk, 
             else { memcpy(qn, qt, sizeof(double) * dk); memcpy(kn, kt, sizeof(double) * dk); }
             /* S <- Diag(alpha_t) S */
             for (int i = 0; i < dk; ++i) {
-                double a = exp(g_min * sigmoid(eA * zt[i]));
+                double a = exp(gate_mode ? -eA * softplus(zt[i]) : g_min * sigmoid(eA * zt[i]));
                 for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] *= a;
             }
             /* u = beta (v - S^T k) */

@@ -3,7 +3,8 @@
 Page: "Kimi K3: KDA, attention residuals and Stable LatentMoE" (hs-black.github.io),
 Sec. 2.1 (recurrence, chunked form), Sec. 2.2 (bounded gate, 16-token
 sub-chunks, e^80 bound), Sec. 2.3 (output gate), Sec. 10.2 (KCP pairs),
-Sec. 13.1 (prefix cache: states restorable at block boundaries).
+Sec. 13.1 (prefix cache: states restorable at block boundaries), and Kimi
+Linear's unbounded gate printed beside K3's in Sec. 2.2.
 
 Each pin is chosen so that a plausible slip in the oracle (a dropped decay, a
 sign, a transposed readout, a wrong index) fails at least one of them; the
@@ -335,6 +336,62 @@ def test_snapshots_are_prefix_states():
 
 
 # --------------------------------------------------------------------------
+# 14. Kimi Linear's gate (Sec. 2.2, the mapping K3 replaces):
+#     g = -exp(A_h) Softplus(z), unbounded below
+# --------------------------------------------------------------------------
+
+def test_softplus_gate_against_logaddexp():
+    z = np.array([-60.0, -30.0, -5.0, -1e-3, 0.0, 1e-3, 0.7, 5.0, 30.0, 60.0])
+    for A in (-1.0, 0.0, 0.5, 2.0):
+        g = oracle.log_decay(z, A, gate="softplus")
+        ref = -np.exp(A) * np.logaddexp(0.0, z)           # Softplus(z) = log(1 + e^z)
+        assert np.allclose(g, ref, rtol=1e-14, atol=0.0)
+        assert np.all(g < 0.0)
+        assert math.isclose(g[4], -math.exp(A) * math.log(2.0), rel_tol=1e-15)
+        assert math.isclose(g[-1], -math.exp(A) * 60.0, rel_tol=1e-15)   # ~ -e^A z for large z
+
+
+def test_softplus_chunked_equals_recurrence():
+    q, k, v, z, beta, A = _rand(150, 2, 16, seed=41, z_std=1.0)
+    o, S_T, _ = oracle.prefill(q, k, v, z, beta, A, gate="softplus", qk_l2norm=False)
+    for h in range(2):
+        g = oracle.log_decay(z[:, h], A[h], gate="softplus")
+        for sub in (None, 16):
+            oc, Sc, _ = chunked.chunked_prefill(q[:, h], k[:, h], v[:, h], g, beta[:, h], np.zeros((16, 16)),
+                                                sub=sub)
+            assert np.allclose(oc, o[:, h], rtol=0, atol=1e-10 * np.abs(o[:, h]).max())
+            assert np.allclose(Sc, S_T[0, h], rtol=0, atol=1e-10 * np.abs(S_T[0, h]).max())
+    # the bounded gate gives a different operator on the same inputs
+    o_b, _, _ = oracle.prefill(q, k, v, z, beta, A, qk_l2norm=False)
+    assert not np.allclose(o_b, o)
+
+
+def test_softplus_gate_breaks_the_subchunk_bound():
+    """With the unbounded gate a single 16-token sub-chunk can hold a cumulative
+    log decay beyond -88.7, so the factored diagonal Gram needs e^(G_a - G_j)
+    above the bf16 / fp32 maximum while the exact per-pair factors stay <= 1
+    and the recurrence stays finite (the page's reason for K3's bound)."""
+    rng = np.random.default_rng(42)
+    T, d = 64, 16
+    q = _unit(rng.standard_normal((T, 1, d)))
+    k = _unit(rng.standard_normal((T, 1, d)))
+    v = rng.standard_normal((T, 1, d))
+    z = 8.0 + rng.standard_normal((T, 1, d))             # Softplus(z) ~ 8 per step
+    beta = np.full((T, 1), 0.5)
+    A = np.zeros(1)
+    g = oracle.log_decay(z[:, 0], A[0], gate="softplus")
+    span = -np.cumsum(g[:16], axis=0)[-1]                   # decay over one sub-chunk
+    assert span.max() > 88.8                                # e^span > bf16 / fp32 max
+    o, S_T, _ = oracle.prefill(q, k, v, z, beta, A, gate="softplus")
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S_T))
+    _, _, fmax = chunked.chunked_prefill(q[:, 0], k[:, 0], v[:, 0], g, beta[:, 0], np.zeros((d, d)), sub=16)
+    assert fmax > float(np.finfo(np.float32).max)
+    gb = oracle.log_decay(z[:, 0], A[0])                    # the bounded gate on the same z
+    _, _, fmax_b = chunked.chunked_prefill(q[:, 0], k[:, 0], v[:, 0], gb, beta[:, 0], np.zeros((d, d)), sub=16)
+    assert fmax_b < math.exp(80.0)
+
+
+# --------------------------------------------------------------------------
 # Mutation check: plant slips in a copy of the C oracle; the pins must notice
 # --------------------------------------------------------------------------
 
@@ -347,6 +404,8 @@ MUTATIONS = {
                                  "(t + 2 - cu_seqlens[n]) % snap_interval == 0"),
     "snapshot_rows_restart": ("snap_row += (cu_seqlens[m + 1] - cu_seqlens[m]) / snap_interval;",
                               "snap_row += 0;"),
+    "softplus_gate_sign": ("return -exp(A_h) * softplus(z);", "return exp(A_h) * softplus(z);"),
+    "softplus_prefill_scale": ("-eA * softplus(zt[i])", "-softplus(zt[i])"),
 }
 
 
@@ -366,14 +425,16 @@ def test_pins_catch_planted_mistakes(name, tmp_path):
         oracle._lib = None
         lib = ctypes.CDLL(str(so))
         oracle._load()  # configure argtypes on the real library, then copy onto the mutant
-        for fn in ("kda_oracle_prefill", "kda_oracle_log_decay", "kda_oracle_gate_norm"):
+        for fn in ("kda_oracle_prefill", "kda_oracle_log_decay", "kda_oracle_log_decay_softplus",
+                   "kda_oracle_gate_norm"):
             getattr(lib, fn).argtypes = getattr(oracle._lib, fn).argtypes
             getattr(lib, fn).restype = getattr(oracle._lib, fn).restype
         oracle._lib = lib
         failed = False
         for pin in (lambda: test_brute_force_rational(4, 4), test_delta_invariant,
                     test_gate_closed_forms, lambda: test_chunked_equals_recurrence(150, 64, 16),
-                    test_snapshots_are_prefix_states):
+                    test_snapshots_are_prefix_states, test_softplus_gate_against_logaddexp,
+                    test_softplus_chunked_equals_recurrence):
             try:
                 pin()
             except AssertionError:
