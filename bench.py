@@ -289,6 +289,20 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     snap_ms = p0.elapsed_time(p1) / args.steps
     del S_snap
+
+    # ---- Kimi Linear's unbounded gate (secondary): the same prefill with
+    # g = -exp(A) Softplus(z), whose diagonal Gram sub-blocks go pair by pair
+    pg_ = kda.PrefillArgs.from_buffer_copy(pa)
+    pg_.gate_mode = kda.GATES["softplus"]
+    for _ in range(max(args.warmup, 3)):
+        kda.prefill_raw(pg_, stream)
+    torch.cuda.synchronize()
+    p0.record(stream)
+    for _ in range(args.steps):
+        kda.prefill_raw(pg_, stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    softplus_ms = p0.elapsed_time(p1) / args.steps
     clocks = sampler.stop()
 
     # ---- end to end: host buffers in, host buffers out, through the public call
@@ -378,6 +392,9 @@ def run_ours(args, rank, world):
                          "snapshot_bytes_per_launch": snap_rows * H * d * d * 4,
                          "ms_per_step": snap_ms, "overhead_vs_plain": snap_ms / ms - 1.0,
                          "value": world * T / (snap_ms * 1e-3), "unit": "tokens/s"},
+        "gate_variant": {"gate": "softplus (Kimi Linear: g = -exp(A) Softplus(z), diagonal Gram pair by pair)",
+                         "ms_per_step": softplus_ms, "time_vs_bounded_gate": softplus_ms / ms,
+                         "value": world * T / (softplus_ms * 1e-3), "unit": "tokens/s"},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,

@@ -52,6 +52,17 @@ typedef enum {
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 
 /*
+ * Decay gate (Sec. 2.2).  KDA_GATE_BOUNDED is K3's g = g_min * Sigmoid(exp(A_h) z),
+ * g in (g_min, 0) -- the operator of this library.  KDA_GATE_SOFTPLUS is the gate
+ * it replaces, Kimi Linear's g = -exp(A_h) * Softplus(z) (g_min unused), unbounded
+ * below: a 16-token sub-chunk can then span more than the bf16/fp32 range, so the
+ * chunked prefill forms the diagonal Gram sub-blocks pair by pair on CUDA cores
+ * (supported by the chunk-parallel schedule and the CUDA-core paths; the
+ * single-pass schedule and kda_prefill_noalloc return KDA_ERR_UNSUPPORTED).
+ */
+typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
+
+/*
  * Chunked prefill over packed sequences (Sec. 2.1 chunked form, Sec. 2.2
  * 16-token sub-chunks; chunk length 64), with optional prefix-cache state
  * snapshots at chunk-aligned intervals (Sec. 13.1: a cached prefix is only
@@ -136,6 +147,7 @@ typedef struct {
      * (and snap_interval unread) when S_snap is NULL. */
     int snap_interval;
     float* S_snap;
+    int gate_mode;        /* kda_gate; KDA_ERR_UNSUPPORTED for other values */
 } kda_prefill_args;
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* args);
@@ -216,6 +228,7 @@ typedef struct {
     const float* norm_w;
     float norm_eps;
     void* y;
+    int gate_mode;        /* kda_gate; KDA_ERR_UNSUPPORTED for other values */
 } kda_decode_args;
 
 kda_status kda_decode_step(const kda_decode_args* args, void* stream);

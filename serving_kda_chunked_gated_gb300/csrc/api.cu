@@ -82,6 +82,7 @@ static kda_status validate_prefill(const kda_prefill_args* a) {
     for (int n = 0; n < a->num_seqs; ++n)
         if (cu[n + 1] < cu[n]) return KDA_ERR_SEQLENS;
     if (cu[a->num_seqs] != a->T_total) return KDA_ERR_SEQLENS;
+    if (a->gate_mode != KDA_GATE_BOUNDED && a->gate_mode != KDA_GATE_SOFTPLUS) return KDA_ERR_UNSUPPORTED;
     if (a->S_snap) {
         if (a->snap_interval <= 0 || a->snap_interval % 64 != 0) return KDA_ERR_SHAPE;
         if (misaligned(a->S_snap)) return KDA_ERR_ALIGN;
@@ -114,6 +115,8 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
         if (misaligned(a->workspace)) return KDA_ERR_ALIGN;
         if (a->workspace_bytes >= kda::prefill_split_workspace_size(*a))
             e = kda::launch_prefill_split(*a, s);
+        else if (a->gate_mode != KDA_GATE_BOUNDED)
+            return KDA_ERR_UNSUPPORTED;   // the single-pass schedule relies on the bounded gate
         else
             e = kda::launch_prefill_tc(*a, s);
     } else {
@@ -132,6 +135,7 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* a, void* stream) {
                  need, KDA_NOALLOC_SCRATCH_BYTES);
         return KDA_ERR_WORKSPACE;
     }
+    if (kda::prefill_tc_supported(*a) && a->gate_mode != KDA_GATE_BOUNDED) return KDA_ERR_UNSUPPORTED;
     if (a->num_seqs == 0) return KDA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = kda::prefill_tc_supported(*a) ? kda::launch_prefill_tc_noalloc(*a, s)
@@ -161,6 +165,7 @@ kda_status kda_decode_step(const kda_decode_args* a, void* stream) {
     if (!a->o && !a->y) return KDA_ERR_NULL;
     if (a->g_in && !a->y) return KDA_ERR_NULL;
     if (a->y && !a->g_in) return KDA_ERR_NULL;
+    if (a->gate_mode != KDA_GATE_BOUNDED && a->gate_mode != KDA_GATE_SOFTPLUS) return KDA_ERR_UNSUPPORTED;
     const void* ptrs[] = {a->q, a->k, a->v, a->z, a->beta, a->A, a->state, a->slots, a->o,
                           a->g_in, a->norm_w, a->y};
     for (const void* p : ptrs)

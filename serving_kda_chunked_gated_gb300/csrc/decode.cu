@@ -43,7 +43,7 @@ decode_step_kernel(kda_decode_args a) {
         const uint16_t* k = reinterpret_cast<const uint16_t*>(a.k) + tok * DEC_D;
         float qi = bf16_to_f(q[tid]), ki = bf16_to_f(k[tid]);
         float zi = a.z[tok * DEC_D + tid];
-        s_alpha[tid] = __expf(log_decay(zi, __expf(a.A[h]), a.g_min));
+        s_alpha[tid] = __expf(log_decay_mode(zi, __expf(a.A[h]), a.g_min, a.gate_mode));
         float qq = warp_sum(qi * qi), kk = warp_sum(ki * ki);
         if (lane == 0) { s_red[0][warp] = qq; s_red[1][warp] = kk; }
         s_q[tid] = qi;

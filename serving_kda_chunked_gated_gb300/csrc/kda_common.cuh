@@ -21,6 +21,16 @@ KDA_DEV float sigmoidf_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)
 // eA is exp(A_h), computed once per head.
 KDA_DEV float log_decay(float z, float eA, float g_min) { return g_min * sigmoidf_fast(eA * z); }
 
+// Kimi Linear's gate, the one K3's replaces (same page, Sec. 2.2):
+//   g = -exp(A_h) * Softplus(z), Softplus(x) = log(1 + e^x), unbounded below.
+KDA_DEV float log_decay_softplus(float z, float eA) {
+    return -eA * (fmaxf(z, 0.f) + log1pf(__expf(-fabsf(z))));
+}
+// gate_mode 0: bounded (K3), 1: softplus (Kimi Linear)
+KDA_DEV float log_decay_mode(float z, float eA, float g_min, int gate_mode) {
+    return gate_mode ? log_decay_softplus(z, eA) : log_decay(z, eA, g_min);
+}
+
 KDA_DEV float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 // round-to-nearest-even float -> bf16 bits (finite inputs)

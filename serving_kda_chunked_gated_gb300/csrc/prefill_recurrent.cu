@@ -54,7 +54,7 @@ prefill_recurrent_kernel(kda_prefill_args a) {
                 ki = reinterpret_cast<const float*>(a.k)[tok * D + tid];
                 s_v[tid] = reinterpret_cast<const float*>(a.v)[tok * D + tid];
             }
-            s_alpha[tid] = __expf(log_decay(a.z[tok * D + tid], eA, a.g_min));
+            s_alpha[tid] = __expf(log_decay_mode(a.z[tok * D + tid], eA, a.g_min, a.gate_mode));
         }
         float qq = warp_sum(qi * qi), kk = warp_sum(ki * ki), kq = warp_sum(qi * ki);
         if (lane == 0) { s_red[0][warp] = qq; s_red[1][warp] = kk; s_red[2][warp] = kq; }

@@ -143,6 +143,26 @@ TC_DEV Loc locate(long rec, int H, const int* cu, const int* cb, int num_seqs) {
     return l;
 }
 
+// Row i and column j (j <= i) of the p-th entry of a 16 x 16 lower triangle, row-major.
+__host__ __device__ constexpr int tri_row(int p) { int i = 0; while ((i + 1) * (i + 2) / 2 <= p) ++i; return i; }
+__host__ __device__ constexpr int tri_col(int p) { return p - tri_row(p) * (tri_row(p) + 1) / 2; }
+
+// Warp reduce-scatter of 32 values: afterwards lane l holds the sum over the
+// warp of v[l] (five exchange rounds, 31 shuffles).  v is overwritten.
+TC_DEV float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < m; ++k) {
+            const float send = up ? v[k] : v[k + m];
+            const float keep = up ? v[k + m] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+    return v[0];
+}
+
 // ---------------------------------------------------------------------------
 // prep: the state-free part of every chunk
 // ---------------------------------------------------------------------------
@@ -163,7 +183,8 @@ constexpr int OFF_RAWV = OFF_KH + TILE_BYTES;       // two [C][64] bf16 tiles, 1
 constexpr int OFF_SMALL = OFF_RAWV + 2 * C * 64 * 2;
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
-              SM_FLOATS = SM_CTAB + NPAIR * D;
+              SM_DIAG = SM_CTAB + NPAIR * D,            // [4 sub-chunks][9 batches][4 warps][32]
+              SM_FLOATS = SM_DIAG + 4 * 9 * 4 * 32;
 constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
 static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0, "swizzled tiles need 1024-B alignment");
 static_assert(2 * D * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
@@ -176,6 +197,9 @@ constexpr uint32_t TM_A2 = 256;  // 64 cols: [T beta ; P beta]
 constexpr uint32_t TM_COLS = 512;
 }  // namespace prep
 
+// GATE 0: K3's bounded gate; 1: Kimi Linear's Softplus gate, whose diagonal Gram
+// sub-blocks are formed pair by pair (their sub-chunk factors can exceed fp32)
+template <int GATE>
 __global__ void __launch_bounds__(NT, 1)
 prep_kernel(kda_prefill_args a, Work w,
             const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -202,6 +226,7 @@ prep_kernel(kda_prefill_args a, Work w,
     float* s_expCE = fs + SM_EXPCE;
     float* s_gam = fs + SM_GAM;
     float* s_ctab = fs + SM_CTAB;
+    float* s_diag = fs + SM_DIAG;
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
     uint64_t* bar_in = mbar + 1;
     uint64_t* bar_v = mbar + 2;
@@ -293,20 +318,25 @@ prep_kernel(kda_prefill_args a, Work w,
             const int d = tid & (D - 1);
 #pragma unroll 1
             for (int b = 2 * (tid >> 7); b < 2 * (tid >> 7) + 2; ++b) {
-                float al[16], kv[16];
-                float F1 = 1.f;
+                float al[16], kv[16], qv[16], Lc[16];
+                float F1 = 1.f, L = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int t = 16 * b + i;
                     float alpha = 1.f, q = 0.f, k = 0.f;
                     if (t < nc) {
-                        alpha = __expf(log_decay(sRawZ[t * D + d], eA, a.g_min));
+                        const float g = GATE ? log_decay_softplus(sRawZ[t * D + d], eA)
+                                             : log_decay(sRawZ[t * D + d], eA, a.g_min);
+                        alpha = __expf(g);
+                        L += g;
                         q = bf16_to_f(sRawQ[t * D + d]) * s_rq[t];
                         k = bf16_to_f(sRawK[t * D + d]) * s_rk[t];
                     }
                     F1 *= alpha;                   // exp(G_t - G_start(b))
                     al[i] = alpha;
                     kv[i] = k;
+                    qv[i] = q;
+                    Lc[i] = L;                     // G_t - G_start(b), log domain
                     sQ[t * QS + d] = q * F1;
                     sKr[t * QS + d] = k * F1;
                 }
@@ -317,6 +347,31 @@ prep_kernel(kda_prefill_args a, Work w,
                     F2 *= al[i];
                 }
                 s_tau[b * D + d] = F1;
+                if (GATE) {
+                    // diagonal sub-block b pair by pair: this channel's share of
+                    // A_qk(i,j) = sum_d q_i k_j exp(G_i - G_j) (j <= i) and of A_kk
+                    // (j < i), 16 pairs per batch, reduce-scattered over the warp's
+                    // 32 channels; the four warps of a sub-chunk add up later
+                    float* dst = s_diag + (b * 9 * 4 + (warp & 3)) * 32 + lane;
+#pragma unroll
+                    for (int bt = 0; bt < 9; ++bt) {
+                        float vals[32];
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int p = 16 * bt + u;
+                            if (p < 136) {
+                                const int i = tri_row(p), j = tri_col(p);
+                                const float kj = (i == j) ? kv[j] : kv[j] * __expf(Lc[i] - Lc[j]);
+                                vals[u] = qv[i] * kj;
+                                vals[16 + u] = (i == j) ? 0.f : kv[i] * kj;
+                            } else {
+                                vals[u] = 0.f;
+                                vals[16 + u] = 0.f;
+                            }
+                        }
+                        dst[bt * 4 * 32] = warp_reduce_scatter32(vals, lane);
+                    }
+                }
             }
         }
         __syncthreads();   // raw q/k/z are dead from here on
@@ -378,7 +433,7 @@ prep_kernel(kda_prefill_args a, Work w,
                 const int k0 = 8 * ks + t4, k1 = k0 + 4;
 #pragma unroll
                 for (int it = 0; it < 3; ++it) {
-                    if (it < 2 || (ks >> 3) == khalf) {
+                    if ((it < 2 || (ks >> 3) == khalf) && !(GATE && ia[it] == ib[it])) {
                         const float* Arows = kk[it] ? sKr : sQ;
                         const int ra = 16 * ia[it] + g;
                         const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
@@ -404,6 +459,7 @@ prep_kernel(kda_prefill_args a, Work w,
                         const int I = 16 * ia[it] + g + 8 * hr;
                         const int J = 16 * ib[it] + 8 * nh + 2 * t4;
                         float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
+                        if (GATE && ia[it] == ib[it]) continue;   // formed pair by pair
                         if (it == 2) {   // raw half-block partial
                             *reinterpret_cast<float2*>(part + warp * 256 + (g + 8 * hr) * 16 + 8 * nh + 2 * t4) =
                                 make_float2(v0, v1);
@@ -420,7 +476,21 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
             }
             __syncthreads();
-            {   // blocks 16..19 = A_kk pairs (3, q), q = 0..3: halves from warps 2q and 2q+1
+            if (GATE) {   // diagonal blocks from the pair-by-pair sums: 2 x 4 blocks of 16 x 16
+#pragma unroll 1
+                for (int x = tid; x < 2 * 4 * 256; x += NT) {
+                    const int kkb = x >> 10, bb = (x >> 8) & 3, i = (x >> 4) & 15, j = x & 15;
+                    float val = 0.f;
+                    if (j <= i && (j < i || !kkb)) {
+                        const int p = i * (i + 1) / 2 + j, bt = p >> 4, slot = (p & 15) + 16 * kkb;
+                        const float* src = s_diag + ((bb * 9 + bt) * 4) * 32 + slot;
+                        val = (src[0] + src[32]) + (src[64] + src[96]);
+                        if (kkb) val *= s_beta[16 * bb + i];
+                    }
+                    (kkb ? sAkk : sAqk)[(16 * bb + i) * AS + 16 * bb + j] = val;
+                }
+            }
+            if (!GATE || (tid >> 6) < 3) {   // blocks 16..19 = A_kk pairs (3, q): halves from warps 2q, 2q+1
                 const int q = tid >> 6, e = (tid & 63) * 4;
                 const int I = 48 + (e >> 4), J = 16 * q + (e & 15);
                 const float4 h0 = *reinterpret_cast<const float4*>(part + (2 * q) * 256 + e);
@@ -1084,8 +1154,11 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(spl::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(spl::prep_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         spl::prep::SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(spl::prep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            spl::prep::SMEM_BYTES);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
@@ -1127,7 +1200,10 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
     if (L.nrec > 0) {
         const int nsm = spl::sm_count();
         const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
-        spl::prep_kernel<<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+        if (a.gate_mode == KDA_GATE_SOFTPLUS)
+            spl::prep_kernel<1><<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+        else
+            spl::prep_kernel<0><<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
         ++launched;
     }
     dim3 grid(spl::SCAN_R, a.H, a.num_seqs);

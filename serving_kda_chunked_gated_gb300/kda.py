@@ -39,7 +39,7 @@ class PrefillArgs(ctypes.Structure):
         ("S0", _vp), ("o", _vp), ("S_T", _vp),
         ("g_in", _vp), ("norm_w", _vp), ("norm_eps", ctypes.c_float), ("y", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-        ("snap_interval", ctypes.c_int), ("S_snap", _vp),
+        ("snap_interval", ctypes.c_int), ("S_snap", _vp), ("gate_mode", ctypes.c_int),
     ]
 
 
@@ -51,7 +51,11 @@ class DecodeArgs(ctypes.Structure):
         ("g_min", ctypes.c_float), ("scale", ctypes.c_float), ("qk_l2norm", ctypes.c_int),
         ("state", _vp), ("slots", _vp), ("o", _vp),
         ("g_in", _vp), ("norm_w", _vp), ("norm_eps", ctypes.c_float), ("y", _vp),
+        ("gate_mode", ctypes.c_int),
     ]
+
+
+GATES = {"bounded": 0, "softplus": 1}   # kda_gate: K3's bounded gate, Kimi Linear's Softplus gate
 
 
 class KDAError(RuntimeError):
@@ -130,7 +134,7 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_seqlens_host, o, S0=None, S_T=None,
                       g_in=None, norm_w=None, y=None, g_min=-5.0, scale=1.0, qk_l2norm=True,
-                      norm_eps=1e-6, workspace=None) -> PrefillArgs:
+                      norm_eps=1e-6, workspace=None, gate="bounded") -> PrefillArgs:
     """Fill the C argument struct from tensors (no validation beyond dtype mapping)."""
     T, H, dk = q.shape
     dv = v.shape[2]
@@ -146,6 +150,7 @@ def make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_seqlens_host, o, S0=No
                     ("y", y)):
         setattr(a, name, t.data_ptr() if t is not None else None)
     a.g_min, a.scale, a.qk_l2norm, a.norm_eps = float(g_min), float(scale), int(bool(qk_l2norm)), float(norm_eps)
+    a.gate_mode = GATES[gate]
     if workspace is not None:
         a.workspace = workspace.data_ptr()
         a.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -180,7 +185,7 @@ def snapshot_count(cu_seqlens_host, interval: int) -> int:
 
 def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
             g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, want_state=True,
-            out=None, stream=None, recurrent=False, workspace=None, snap_interval=0):
+            out=None, stream=None, recurrent=False, workspace=None, snap_interval=0, gate="bounded"):
     """KDA chunked prefill through ``kda_prefill``.
 
     q, k, z: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; A: [H]; cu_seqlens: int32
@@ -202,7 +207,7 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
         y = out["y"] if out else torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev)
     args = make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_host, o, S0=S0, S_T=S_T,
                              g_in=g_in, norm_w=norm_w, y=y, g_min=g_min, scale=scale,
-                             qk_l2norm=qk_l2norm, norm_eps=norm_eps)
+                             qk_l2norm=qk_l2norm, norm_eps=norm_eps, gate=gate)
     S_snap = None
     if snap_interval:
         rows = snapshot_count(cu_host.tolist(), snap_interval)
@@ -226,7 +231,8 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
 
 
 def make_decode_args(q, k, v, z, beta, A, state, o=None, y=None, g_in=None, norm_w=None,
-                     slots=None, g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6) -> DecodeArgs:
+                     slots=None, g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6,
+                     gate="bounded") -> DecodeArgs:
     N, H, dk = q.shape
     a = DecodeArgs()
     a.N, a.H, a.dk, a.dv = int(N), int(H), int(dk), int(v.shape[2])
@@ -236,6 +242,7 @@ def make_decode_args(q, k, v, z, beta, A, state, o=None, y=None, g_in=None, norm
                     ("norm_w", norm_w), ("y", y)):
         setattr(a, name, t.data_ptr() if t is not None else None)
     a.g_min, a.scale, a.qk_l2norm, a.norm_eps = float(g_min), float(scale), int(bool(qk_l2norm)), float(norm_eps)
+    a.gate_mode = GATES[gate]
     return a
 
 
@@ -244,7 +251,7 @@ def decode_step_raw(args: DecodeArgs, stream=None):
 
 
 def decode_step(q, k, v, z, beta, A, state, g_in=None, norm_w=None, slots=None, want_o=True,
-                g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, stream=None):
+                g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, stream=None, gate="bounded"):
     """One decode step through ``kda_decode_step``; ``state`` is updated in place.
 
     Returns (o or None, y or None).
@@ -255,7 +262,7 @@ def decode_step(q, k, v, z, beta, A, state, g_in=None, norm_w=None, slots=None, 
     y = torch.empty((N, H, dv), dtype=torch.bfloat16, device=q.device) if g_in is not None else None
     args = make_decode_args(q, k, v, z, beta, A, state, o=o, y=y, g_in=g_in, norm_w=norm_w,
                             slots=slots, g_min=g_min, scale=scale, qk_l2norm=qk_l2norm,
-                            norm_eps=norm_eps)
+                            norm_eps=norm_eps, gate=gate)
     decode_step_raw(args, stream)
     return o, y
 
