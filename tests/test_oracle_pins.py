@@ -3,8 +3,9 @@
 Page: "Kimi K3: KDA, attention residuals and Stable LatentMoE" (hs-black.github.io),
 Sec. 2.1 (recurrence, chunked form), Sec. 2.2 (bounded gate, 16-token
 sub-chunks, e^80 bound), Sec. 2.3 (output gate), Sec. 10.2 (KCP pairs),
-Sec. 13.1 (prefix cache: states restorable at block boundaries), and Kimi
-Linear's unbounded gate printed beside K3's in Sec. 2.2.
+Sec. 13.1 (prefix cache: states restorable at block boundaries), Kimi
+Linear's unbounded gate printed beside K3's in Sec. 2.2, and the ShortConv +
+Swish prologue of Sec. 2.1.
 
 Each pin is chosen so that a plausible slip in the oracle (a dropped decay, a
 sign, a transposed readout, a wrong index) fails at least one of them; the
@@ -389,6 +390,70 @@ def test_softplus_gate_breaks_the_subchunk_bound():
     gb = oracle.log_decay(z[:, 0], A[0])                    # the bounded gate on the same z
     _, _, fmax_b = chunked.chunked_prefill(q[:, 0], k[:, 0], v[:, 0], gb, beta[:, 0], np.zeros((d, d)), sub=16)
     assert fmax_b < math.exp(80.0)
+
+
+# --------------------------------------------------------------------------
+# 15. ShortConv + Swish prologue (Sec. 2.1; Swish of Sec. 5): causal depthwise
+#     conv with a conv state, pinned to library routines and invariants
+# --------------------------------------------------------------------------
+
+def test_short_conv_equals_numpy_convolve_and_expit():
+    from scipy.special import expit
+    from oracle import prologue
+    rng = np.random.default_rng(51)
+    T, C, W = 37, 6, 4
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    y, st = prologue.short_conv(x, w, activation=False)
+    for c in range(C):   # causal FIR with zero history: full convolution, first T outputs
+        np.testing.assert_allclose(y[:, c], np.convolve(x[:, c], w[c, ::-1])[:T], rtol=0, atol=1e-12)
+    assert np.array_equal(st[0], x[T - (W - 1):])            # state = the last W-1 inputs
+    b = rng.standard_normal(C)
+    ys, _ = prologue.short_conv(x, w, b)
+    np.testing.assert_allclose(ys, (y + b) * expit(y + b), rtol=1e-14, atol=1e-14)
+    z = np.linspace(-40, 40, 81)
+    np.testing.assert_allclose(prologue.swish(z), z * expit(z), rtol=1e-14, atol=1e-300)
+
+
+def test_short_conv_width_one_is_pointwise():
+    from oracle import prologue
+    rng = np.random.default_rng(52)
+    x = rng.standard_normal((10, 5))
+    w = rng.standard_normal((5, 1))
+    b = rng.standard_normal(5)
+    y, st = prologue.short_conv(x, w, b)
+    pre = x * w[:, 0] + b
+    np.testing.assert_allclose(y, pre / (1 + np.exp(-pre)), rtol=1e-14)
+    assert st.shape == (1, 0, 5)
+
+
+def test_short_conv_state_continuity_varlen_and_decode():
+    from oracle import prologue
+    rng = np.random.default_rng(53)
+    T, C, W = 50, 7, 4
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    b = rng.standard_normal(C)
+    s0 = rng.standard_normal((1, W - 1, C))
+    y, st = prologue.short_conv(x, w, b, state=s0)
+    for a in (1, 2, 3, 17):                                   # splits shorter and longer than W-1
+        y1, s1 = prologue.short_conv(x[:a], w, b, state=s0)
+        y2, s2 = prologue.short_conv(x[a:], w, b, state=s1)
+        assert np.array_equal(np.concatenate([y1, y2]), y) and np.array_equal(s2, st)
+    # packed sequences equal separate calls
+    cu = np.array([0, 0, 2, 20, 50])
+    S0 = rng.standard_normal((4, W - 1, C))
+    yp, sp = prologue.short_conv(x, w, b, cu_seqlens=cu, state=S0)
+    for n in range(4):
+        yn, sn = prologue.short_conv(x[cu[n]:cu[n + 1]], w, b, state=S0[n:n + 1])
+        assert np.array_equal(yp[cu[n]:cu[n + 1]], yn) and np.array_equal(sp[n], sn[0])
+    assert np.array_equal(sp[0], S0[0])                        # an empty sequence keeps its state
+    # decode steps continue a prefill
+    yd, sd = prologue.short_conv(x[:30], w, b, state=s0)
+    for t in range(30, T):
+        yt, sd = prologue.short_conv_step(x[t:t + 1], w, b, state=sd)
+        assert np.array_equal(yt[0], y[t])
+    assert np.array_equal(sd, st)
 
 
 # --------------------------------------------------------------------------
