@@ -35,6 +35,7 @@ METRIC = "KDA prefill tokens/s (% BF16 TC peak); decode-step HBM GB/s (% of peak
 FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 128 * 65 + 64 * 64 // 3
 TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 : bf16 ratio (GB300)
 SNAP_INTERVAL = 1024            # prefix-cache block: one state snapshot per 1024 tokens
+PROLOGUE_WIDTH = 4              # ShortConv width (not given by the KDA pages; a parameter)
 
 WORKLOADS = {
     "prefill_128k": dict(T=131072, H=32, d=128, S0=True, gate=True, varlen=None),
@@ -303,6 +304,33 @@ def run_ours(args, rank, world):
     p1.record(stream)
     torch.cuda.synchronize()
     softplus_ms = p0.elapsed_time(p1) / args.steps
+
+    # ---- ShortConv + Swish prologue (secondary): q, k, v pre-activations [T, H*d]
+    # bf16 through a width-4 causal depthwise conv with conv states in and out
+    Cc, Wc = H * d, PROLOGUE_WIDTH
+    gen = torch.Generator(device=dev).manual_seed(77 + rank)
+    cu_dev = inp["cu_seqlens"]
+    pro = []
+    for _ in range(3):
+        xp = torch.randn((T, Cc), generator=gen, device=dev).to(torch.bfloat16)
+        wp = (torch.randn((Cc, Wc), generator=gen, device=dev) / Wc).float()
+        si = torch.randn((N, Wc - 1, Cc), generator=gen, device=dev).float()
+        yp, so = torch.empty_like(xp), torch.empty_like(si)
+        pro.append((kda.make_short_conv_args(xp, wp, yp, cu_dev, cu_host, state_in=si, state_out=so),
+                    (xp, wp, si, yp, so)))
+    for _ in range(max(args.warmup, 3)):
+        for pa_, _keep in pro:
+            kda.short_conv_raw(pa_, stream)
+    torch.cuda.synchronize()
+    p0.record(stream)
+    for _ in range(args.steps):
+        for pa_, _keep in pro:
+            kda.short_conv_raw(pa_, stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    pro_ms = p0.elapsed_time(p1) / args.steps
+    pro_bytes = 3 * (2 * T * Cc * 2 + 2 * N * (Wc - 1) * Cc * 4 + Cc * Wc * 4)
+    del pro
     clocks = sampler.stop()
 
     # ---- end to end: host buffers in, host buffers out, through the public call
@@ -395,6 +423,12 @@ def run_ours(args, rank, world):
         "gate_variant": {"gate": "softplus (Kimi Linear: g = -exp(A) Softplus(z), diagonal Gram pair by pair)",
                          "ms_per_step": softplus_ms, "time_vs_bounded_gate": softplus_ms / ms,
                          "value": world * T / (softplus_ms * 1e-3), "unit": "tokens/s"},
+        "prologue": {"op": "ShortConv (width %d) + Swish on q, k, v [T, H*d] bf16, conv states in/out" % PROLOGUE_WIDTH,
+                     "ms_per_step": pro_ms,
+                     "roofline": {"bound": "hbm", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9, "peak": pk["hbm"],
+                                  "unit": "GB/s", "frac": pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm"],
+                                  "algorithmic_bytes_per_launch": pro_bytes,
+                                  "launch": "three kda_short_conv calls (q, k, v)"}},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,

@@ -243,6 +243,67 @@ kda_status kda_decode_step(const kda_decode_args* args, void* stream);
 kda_status kda_gate_norm(const void* o, const void* g_in, const float* norm_w, float eps,
                          void* y, long rows, int dv, kda_dtype dtype, void* stream);
 
+/*
+ * ShortConv + Swish prologue (Sec. 2.1: q and k pass through ShortConv, Swish
+ * and L2Norm before the recurrence, v through ShortConv and Swish; Sec. 5:
+ * Swish(z) = z * Sigmoid(z); "Kimi-K3 深度技术分析" (liuhc.cn), prefill-decode
+ * section: decode keeps a sliding-window state of the convolution).  The pages
+ * give no width; any W in 1..8.  Per channel c of each packed sequence n:
+ *   pre[t, c] = sum_{i=0}^{W-1} weight[c*W + i] * x[t - (W-1) + i, c] + bias[c]
+ *   y[t, c]   = Swish(pre[t, c])  (activation = 1)  or  pre[t, c]  (activation = 0)
+ * where positions before the sequence's first token read state_in[n] (the W-1
+ * inputs that preceded it, oldest first; zeros when state_in is NULL), and
+ * state_out[n] receives the last W-1 entries of [state_in[n], x of sequence n].
+ *   x, y                 [T_total, channels]  dtype (bf16 or float32; y != x)
+ *   weight               [channels, W] float32;  bias [channels] float32 or NULL
+ *   state_in, state_out  [num_seqs, W-1, channels] float32 or NULL (must differ)
+ * cu_seqlens / cu_seqlens_host as for kda_prefill.  channels: a multiple of 8.
+ * The L2Norm of q and k is kda_prefill's qk_l2norm.  Errors: KDA_ERR_SHAPE
+ * (width, channels), KDA_ERR_SEQLENS, KDA_ERR_NULL, KDA_ERR_ALIGN (16 bytes),
+ * KDA_ERR_DTYPE.
+ */
+typedef struct {
+    int num_seqs;
+    int T_total;
+    int channels;
+    int width;
+    kda_dtype dtype;
+    const int32_t* cu_seqlens;       /* device */
+    const int32_t* cu_seqlens_host;  /* host   */
+    const void* x;
+    const float* weight;
+    const float* bias;
+    const float* state_in;
+    float* state_out;
+    void* y;
+    int activation;
+} kda_short_conv_args;
+
+kda_status kda_short_conv(const kda_short_conv_args* args, void* stream);
+
+/*
+ * One decode step of the prologue: x, y [N, channels] (one token per sequence),
+ * state [num_slots, W-1, channels] float32 updated in place (row slots[i] for
+ * token i, or row i when slots is NULL; slots must be distinct):
+ *   y = Swish(conv([state, x]))  then  state <- last W-1 entries of [state, x].
+ */
+typedef struct {
+    int N;
+    int channels;
+    int width;
+    int num_slots;
+    kda_dtype dtype;
+    const void* x;
+    const float* weight;
+    const float* bias;
+    float* state;
+    const int32_t* slots;
+    void* y;
+    int activation;
+} kda_short_conv_step_args;
+
+kda_status kda_short_conv_step(const kda_short_conv_step_args* args, void* stream);
+
 /* Static description of a status code. */
 const char* kda_status_str(kda_status s);
 

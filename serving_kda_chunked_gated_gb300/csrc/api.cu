@@ -18,6 +18,8 @@ size_t prefill_tc_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_split_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s);
+cudaError_t launch_short_conv(const kda_short_conv_args& a, cudaStream_t s);
+cudaError_t launch_short_conv_step(const kda_short_conv_step_args& a, cudaStream_t s);
 }  // namespace kda
 
 static thread_local char g_last_error[256] = "no error";
@@ -148,6 +150,46 @@ kda_status kda_prefill_recurrent(const kda_prefill_args* a, void* stream) {
     if (st != KDA_OK) return st;
     if (a->num_seqs == 0) return KDA_OK;
     cudaError_t e = kda::launch_prefill_recurrent(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// ShortConv + Swish prologue
+// ---------------------------------------------------------------------------
+
+kda_status kda_short_conv(const kda_short_conv_args* a, void* stream) {
+    if (!a) return KDA_ERR_NULL;
+    if (a->num_seqs < 0 || a->T_total < 0 || a->channels <= 0 || a->channels % 8 != 0) return KDA_ERR_SHAPE;
+    if (a->width < 1 || a->width > 8) return KDA_ERR_SHAPE;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!a->cu_seqlens || !a->cu_seqlens_host) return KDA_ERR_NULL;
+    if (a->T_total > 0 && (!a->x || !a->y || !a->weight)) return KDA_ERR_NULL;
+    if (a->x && a->x == a->y) return KDA_ERR_SHAPE;
+    if (a->state_in && a->state_in == a->state_out) return KDA_ERR_SHAPE;
+    const void* ptrs[] = {a->x, a->y, a->weight, a->bias, a->state_in, a->state_out, a->cu_seqlens};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return KDA_ERR_ALIGN;
+    const int32_t* cu = a->cu_seqlens_host;
+    if (cu[0] != 0) return KDA_ERR_SEQLENS;
+    for (int n = 0; n < a->num_seqs; ++n)
+        if (cu[n + 1] < cu[n]) return KDA_ERR_SEQLENS;
+    if (cu[a->num_seqs] != a->T_total) return KDA_ERR_SEQLENS;
+    if (a->num_seqs == 0) return KDA_OK;
+    cudaError_t e = kda::launch_short_conv(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+kda_status kda_short_conv_step(const kda_short_conv_step_args* a, void* stream) {
+    if (!a) return KDA_ERR_NULL;
+    if (a->N < 0 || a->num_slots < 0 || a->channels <= 0 || a->channels % 8 != 0) return KDA_ERR_SHAPE;
+    if (a->width < 1 || a->width > 8) return KDA_ERR_SHAPE;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_F32) return KDA_ERR_DTYPE;
+    if (!a->slots && a->num_slots < a->N) return KDA_ERR_SHAPE;
+    if (a->N > 0 && (!a->x || !a->y || !a->weight || (a->width > 1 && !a->state))) return KDA_ERR_NULL;
+    const void* ptrs[] = {a->x, a->y, a->weight, a->bias, a->state, a->slots};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return KDA_ERR_ALIGN;
+    cudaError_t e = kda::launch_short_conv_step(*a, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : cuda_fail(e);
 }
 

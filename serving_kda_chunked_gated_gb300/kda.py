@@ -23,7 +23,8 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
-            "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count"]
+            "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count",
+            "kda_short_conv", "kda_short_conv_step"]
 
 _vp = ctypes.c_void_p
 
@@ -58,6 +59,25 @@ class DecodeArgs(ctypes.Structure):
 GATES = {"bounded": 0, "softplus": 1}   # kda_gate: K3's bounded gate, Kimi Linear's Softplus gate
 
 
+class ShortConvArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int), ("T_total", ctypes.c_int), ("channels", ctypes.c_int),
+        ("width", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("cu_seqlens", _vp), ("cu_seqlens_host", _vp),
+        ("x", _vp), ("weight", _vp), ("bias", _vp), ("state_in", _vp), ("state_out", _vp),
+        ("y", _vp), ("activation", ctypes.c_int),
+    ]
+
+
+class ShortConvStepArgs(ctypes.Structure):
+    _fields_ = [
+        ("N", ctypes.c_int), ("channels", ctypes.c_int), ("width", ctypes.c_int), ("num_slots", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("x", _vp), ("weight", _vp), ("bias", _vp), ("state", _vp), ("slots", _vp),
+        ("y", _vp), ("activation", ctypes.c_int),
+    ]
+
+
 class KDAError(RuntimeError):
     pass
 
@@ -85,6 +105,10 @@ def load_library(path: str = LIB_PATH):
     lib.kda_prefill_snapshot_count.argtypes = [ctypes.POINTER(PrefillArgs)]
     lib.kda_prefill_snapshot_count.restype = ctypes.c_long
     lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+    lib.kda_short_conv.restype = ctypes.c_int
+    lib.kda_short_conv.argtypes = [ctypes.POINTER(ShortConvArgs), _vp]
+    lib.kda_short_conv_step.restype = ctypes.c_int
+    lib.kda_short_conv_step.argtypes = [ctypes.POINTER(ShortConvStepArgs), _vp]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_gate_norm.argtypes = [_vp, _vp, _vp, ctypes.c_float, _vp, ctypes.c_long,
                                   ctypes.c_int, ctypes.c_int, _vp]
@@ -265,6 +289,64 @@ def decode_step(q, k, v, z, beta, A, state, g_in=None, norm_w=None, slots=None, 
                             norm_eps=norm_eps, gate=gate)
     decode_step_raw(args, stream)
     return o, y
+
+
+def make_short_conv_args(x, weight, y, cu_seqlens, cu_seqlens_host, bias=None, state_in=None,
+                         state_out=None, activation=True) -> ShortConvArgs:
+    a = ShortConvArgs()
+    a.num_seqs = int(cu_seqlens_host.numel() - 1)
+    a.T_total, a.channels = int(x.shape[0]), int(x.shape[1])
+    a.width = int(weight.shape[1])
+    a.dtype = _dtype_code(x)
+    a.cu_seqlens, a.cu_seqlens_host = cu_seqlens.data_ptr(), cu_seqlens_host.data_ptr()
+    for name, t in (("x", x), ("weight", weight), ("bias", bias), ("state_in", state_in),
+                    ("state_out", state_out), ("y", y)):
+        setattr(a, name, t.data_ptr() if t is not None else None)
+    a.activation = int(bool(activation))
+    return a
+
+
+def short_conv_raw(args: ShortConvArgs, stream=None):
+    _check(load_library().kda_short_conv(ctypes.byref(args), _stream(stream)), "kda_short_conv")
+
+
+def short_conv(x, weight, bias=None, cu_seqlens=None, state_in=None, want_state=True, activation=True,
+               stream=None):
+    """ShortConv + Swish prologue through ``kda_short_conv``.
+
+    x: [T, C] (bf16 or f32); weight [C, W] f32; bias [C] or None; cu_seqlens int32
+    [N+1] on the device (None = one sequence); state_in [N, W-1, C] f32 or None.
+    Returns (y [T, C] in x's dtype, state_out [N, W-1, C] or None).
+    """
+    T, C = x.shape
+    W = weight.shape[1]
+    dev = x.device
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    cu_host = cu_seqlens.to("cpu")
+    N = cu_host.numel() - 1
+    y = torch.empty_like(x)
+    state_out = torch.empty((N, W - 1, C), dtype=torch.float32, device=dev) if (want_state and W > 1) else None
+    args = make_short_conv_args(x, weight, y, cu_seqlens, cu_host, bias=bias, state_in=state_in,
+                                state_out=state_out, activation=activation)
+    short_conv_raw(args, stream)
+    return y, state_out
+
+
+def short_conv_step(x, weight, state, bias=None, slots=None, activation=True, stream=None):
+    """One decode step of the prologue through ``kda_short_conv_step``; ``state``
+    [S, W-1, C] is updated in place.  Returns y [N, C]."""
+    N, C = x.shape
+    a = ShortConvStepArgs()
+    a.N, a.channels, a.width = int(N), int(C), int(weight.shape[1])
+    a.num_slots = int(state.shape[0]) if state is not None else 0
+    a.dtype = _dtype_code(x)
+    y = torch.empty_like(x)
+    for name, t in (("x", x), ("weight", weight), ("bias", bias), ("state", state), ("slots", slots), ("y", y)):
+        setattr(a, name, t.data_ptr() if t is not None else None)
+    a.activation = int(bool(activation))
+    _check(load_library().kda_short_conv_step(ctypes.byref(a), _stream(stream)), "kda_short_conv_step")
+    return y
 
 
 def gate_norm(o, g_in, norm_w=None, eps=1e-6, out=None, stream=None):

@@ -30,23 +30,25 @@ def test_every_declared_symbol_is_exported(kda_lib):
 
 def test_struct_layout_matches_c(tmp_path):
     import serving_kda_chunked_gated_gb300.kda as kda
+    structs = [("kda_prefill_args", kda.PrefillArgs), ("kda_decode_args", kda.DecodeArgs),
+               ("kda_short_conv_args", kda.ShortConvArgs), ("kda_short_conv_step_args", kda.ShortConvStepArgs)]
     prog = tmp_path / "layout.c"
-    fields_p = [f[0] for f in kda.PrefillArgs._fields_]
-    fields_d = [f[0] for f in kda.DecodeArgs._fields_]
-    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
-             'printf("%zu %zu\\n", sizeof(kda_prefill_args), sizeof(kda_decode_args));']
-    lines += [f'printf("%zu\\n", offsetof(kda_prefill_args, {f}));' for f in fields_p]
-    lines += [f'printf("%zu\\n", offsetof(kda_decode_args, {f}));' for f in fields_d]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){"]
+    for cname, py in structs:
+        lines.append(f'printf("%zu\\n", sizeof({cname}));')
+        lines += [f'printf("%zu\\n", offsetof({cname}, {f[0]}));' for f in py._fields_]
     lines += ["return 0;}"]
     prog.write_text("\n".join(lines))
     exe = tmp_path / "layout"
     subprocess.run(["gcc", str(prog), "-o", str(exe)], check=True)
-    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
-    sp, sd = int(out[0]), int(out[1])
-    offs = [int(x) for x in out[2:]]
-    assert sp == ctypes.sizeof(kda.PrefillArgs) and sd == ctypes.sizeof(kda.DecodeArgs)
-    assert offs[:len(fields_p)] == [getattr(kda.PrefillArgs, f).offset for f in fields_p]
-    assert offs[len(fields_p):] == [getattr(kda.DecodeArgs, f).offset for f in fields_d]
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    i = 0
+    for cname, py in structs:
+        assert out[i] == ctypes.sizeof(py), cname
+        i += 1
+        for f in py._fields_:
+            assert out[i] == getattr(py, f[0]).offset, (cname, f[0])
+            i += 1
 
 
 FAKE = 0x7f0000000000  # never dereferenced: validation fails before any launch
@@ -140,6 +142,27 @@ def test_decode_and_gate_norm_validation(kda_lib):
     assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 128, 9, None) == 3
     assert f(None, FAKE, None, 1e-6, FAKE, 10, 128, 0, None) == 1
     assert f(FAKE + 2, FAKE, None, 1e-6, FAKE, 10, 128, 0, None) == 4
+
+
+def test_short_conv_validation(kda_lib):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    cu = np.array([0, 64], dtype=np.int32)
+    a = kda.ShortConvArgs()
+    a.num_seqs, a.T_total, a.channels, a.width, a.dtype = 1, 64, 256, 4, kda.KDA_BF16
+    a.cu_seqlens, a.cu_seqlens_host = FAKE, cu.ctypes.data
+    a.x, a.weight, a.y, a.activation = FAKE, FAKE + 4096, FAKE + 8192, 1
+    f = kda_lib.kda_short_conv
+    for field, val, expect in (("width", 9, 2), ("width", 0, 2), ("channels", 100, 2), ("dtype", 7, 3),
+                               ("y", FAKE, 2), ("x", FAKE + 8, 4), ("T_total", 65, 5), ("weight", None, 1)):
+        b = kda.ShortConvArgs.from_buffer_copy(a)
+        setattr(b, field, val)
+        assert f(ctypes.byref(b), None) == expect, (field, val)
+    st = kda.ShortConvStepArgs()
+    st.N, st.channels, st.width, st.num_slots, st.dtype = 4, 256, 4, 2, kda.KDA_BF16
+    st.x, st.weight, st.y, st.state = FAKE, FAKE, FAKE, FAKE
+    assert kda_lib.kda_short_conv_step(ctypes.byref(st), None) == 2     # fewer state rows than tokens
+    st.num_slots, st.state = 4, None
+    assert kda_lib.kda_short_conv_step(ctypes.byref(st), None) == 1     # width > 1 needs a state
 
 
 def test_status_strings(kda_lib):
