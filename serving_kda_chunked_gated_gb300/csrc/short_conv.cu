@@ -97,16 +97,9 @@ __global__ void __launch_bounds__(NT) short_conv_kernel(kda_short_conv_args a) {
         }
     };
     fill(t_begin);
-#pragma unroll 1
-    for (int t = t_begin; t < t_end; ++t) {
-        if (t >= s_end) {   // the next sequence starts here (skip empty ones)
-            while (t >= a.cu_seqlens[n + 1]) ++n;
-            s_start = a.cu_seqlens[n];
-            s_end = a.cu_seqlens[n + 1];
-            fill(t);
-        }
-        float xv[8], y[8];
-        load8<BF16>(a.x, (size_t)t * C + c0, xv);
+    // one token: y from the window and x, then slide the window
+    auto step = [&](int t, const float* xv) {
+        float y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float pre = fmaf(wt[W - 1][j], xv[j], bs[j]);
@@ -122,6 +115,33 @@ __global__ void __launch_bounds__(NT) short_conv_kernel(kda_short_conv_args a) {
         if (W > 1) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) hist[W > 1 ? W - 2 : 0][j] = xv[j];
+        }
+    };
+    int t = t_begin;
+#pragma unroll 1
+    while (t < t_end) {
+        if (t >= s_end) {   // the next sequence starts here (skip empty ones)
+            while (t >= a.cu_seqlens[n + 1]) ++n;
+            s_start = a.cu_seqlens[n];
+            s_end = a.cu_seqlens[n + 1];
+            fill(t);
+        }
+        const int stop = min(t_end, s_end);   // this sequence's tokens in the segment
+        // U tokens per round: their loads are issued together, then consumed in order
+        constexpr int U = 4;
+#pragma unroll 1
+        for (; t + U <= stop; t += U) {
+            float xv[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) load8<BF16>(a.x, (size_t)(t + u) * C + c0, xv[u]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) step(t + u, xv[u]);
+        }
+#pragma unroll 1
+        for (; t < stop; ++t) {
+            float xv[8];
+            load8<BF16>(a.x, (size_t)t * C + c0, xv);
+            step(t, xv);
         }
     }
 }
