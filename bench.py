@@ -36,6 +36,7 @@ FLOP_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 128 * 65 + 64 * 64 // 3
 TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 : bf16 ratio (GB300)
 SNAP_INTERVAL = 1024            # prefix-cache block: one state snapshot per 1024 tokens
 PROLOGUE_WIDTH = 4              # ShortConv width (not given by the KDA pages; a parameter)
+KCP_RANKS = 8                   # context-parallel split measured by the KCP secondary
 
 WORKLOADS = {
     "prefill_128k": dict(T=131072, H=32, d=128, S0=True, gate=True, varlen=None),
@@ -331,6 +332,39 @@ def run_ours(args, rank, world):
     pro_ms = p0.elapsed_time(p1) / args.steps
     pro_bytes = 3 * (2 * T * Cc * 2 + 2 * N * (Wc - 1) * Cc * 4 + Cc * Wc * 4)
     del pro
+
+    # ---- KDA context parallelism (secondary): one rank's work when the sequence
+    # is split over KCP_RANKS GPUs -- its transition pair (two state-only
+    # prefills), the entry state from the other ranks' pairs, then its segment
+    kcp_res = None
+    if N == 1 and T % KCP_RANKS == 0:
+        from serving_kda_chunked_gated_gb300 import kcp as kcp_mod
+        Ts = T // KCP_RANKS
+        seg = {key: inp[key][T - Ts:] for key in ("q", "k", "v", "z", "beta")}
+        seg["A"] = inp["A"]
+        ops = kcp_mod.GpuOps()
+        S_zero = torch.zeros((H, d, d), dtype=torch.float32, device=dev)
+
+        def rank_work():
+            M_, St_ = ops.pair(seg)
+            # the last rank folds KCP_RANKS - 1 gathered pairs; this segment's own
+            # pair stands in for them (same shapes, same cost)
+            S_e = kcp_mod.entry_state([(M_, St_)] * (KCP_RANKS - 1), S_zero, ops)
+            return ops.prefill(seg, S_e)
+        for _ in range(2):
+            rank_work()
+        torch.cuda.synchronize()
+        p0.record(stream)
+        for _ in range(args.steps):
+            rank_work()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        kcp_ms = p0.elapsed_time(p1) / args.steps
+        kcp_res = {"ranks": KCP_RANKS, "segment_tokens": Ts, "rank_work_ms": kcp_ms,
+                   "allgather_bytes_per_rank": H * d * (2 * d) * 4,
+                   "time_vs_one_gpu": kcp_ms / ms,
+                   "note": "the last rank's work measured on this GPU; ranks run concurrently on separate GPUs "
+                           "and the all-gather is not timed here"}
     clocks = sampler.stop()
 
     # ---- end to end: host buffers in, host buffers out, through the public call
@@ -429,6 +463,7 @@ def run_ours(args, rank, world):
                                   "unit": "GB/s", "frac": pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm"],
                                   "algorithmic_bytes_per_launch": pro_bytes,
                                   "launch": "three kda_short_conv calls (q, k, v)"}},
+        "kcp": kcp_res,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,

@@ -84,7 +84,8 @@ typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
  *   beta  [T_total, H]       float32  write strengths in (0, 1)
  *   A     [H]                float32  per-head log scale
  *   S0    [num_seqs, H, dk, dv] float32 initial states, or NULL (zero state)
- *   o     [T_total, H, dv]   dtype qkv_dtype (output)
+ *   o     [T_total, H, dv]   dtype qkv_dtype (output), or NULL when only the
+ *         final states are wanted (e.g. the KCP transition pairs below)
  *   S_T   [num_seqs, H, dk, dv] float32 final states (output), or NULL;
  *         S_T may equal S0 (in-place state update).
  *   g_in  [T_total, H, dv]   bf16 gate pre-activations, or NULL (no fused gate)
@@ -303,6 +304,21 @@ typedef struct {
 } kda_short_conv_step_args;
 
 kda_status kda_short_conv_step(const kda_short_conv_step_args* args, void* stream);
+
+/*
+ * KDA context parallelism (Sec. 10.2): a segment acts on the state as
+ * S_exit = M S_entry + S~ with M = M_T ... M_1, M_t = (I - beta_t k_t k_t^T)
+ * Diag(alpha_t), and S~ the segment's state from zero.  Both come from
+ * kda_prefill run state-only (o = NULL): M is the final state with v = 0 and
+ * S0 = I (dv = dk), S~ the final state with S0 = NULL.  A rank's entry state is
+ * the earlier segments' pairs applied in order, S <- M_j S + S~_j, and pairs
+ * compose as (M2, S2) o (M1, S1) = (M2 M1, S2 + M2 S1).
+ *
+ * kda_kcp_apply: for every head h, X[h] <- M[h] X[h] + add[h], in FP32.
+ *   M [H, d, d], X [H, d, n] (in/out), add [H, d, n] or NULL; X must not
+ *   overlap M or add; 1 <= d <= 256, n >= 1; all device memory, 16-byte aligned.
+ */
+kda_status kda_kcp_apply(const float* M, float* X, const float* add, int H, int d, int n, void* stream);
 
 /* Static description of a status code. */
 const char* kda_status_str(kda_status s);

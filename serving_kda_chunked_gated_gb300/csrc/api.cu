@@ -19,6 +19,7 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_split_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s);
 cudaError_t launch_short_conv(const kda_short_conv_args& a, cudaStream_t s);
+cudaError_t launch_kcp_apply(const float* M, float* X, const float* Add, int H, int d, int n, cudaStream_t s);
 cudaError_t launch_short_conv_step(const kda_short_conv_step_args& a, cudaStream_t s);
 }  // namespace kda
 
@@ -71,7 +72,7 @@ static kda_status validate_prefill(const kda_prefill_args* a) {
     if (a->qkv_dtype != KDA_BF16 && a->qkv_dtype != KDA_F32) return KDA_ERR_DTYPE;
     if (!(a->dk == 32 || a->dk == 64 || a->dk == 128)) return KDA_ERR_SHAPE;
     if (!a->cu_seqlens || !a->cu_seqlens_host) return KDA_ERR_NULL;
-    if (a->T_total > 0 && (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o)) return KDA_ERR_NULL;
+    if (a->T_total > 0 && (!a->q || !a->k || !a->v || !a->z || !a->beta)) return KDA_ERR_NULL;
     if (!a->A) return KDA_ERR_NULL;
     if (a->g_in && !a->y) return KDA_ERR_NULL;
     if (a->g_in && a->qkv_dtype != KDA_BF16) return KDA_ERR_DTYPE;
@@ -190,6 +191,19 @@ kda_status kda_short_conv_step(const kda_short_conv_step_args* a, void* stream) 
     for (const void* p : ptrs)
         if (misaligned(p)) return KDA_ERR_ALIGN;
     cudaError_t e = kda::launch_short_conv_step(*a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// context parallelism: apply a segment's transition pair
+// ---------------------------------------------------------------------------
+
+kda_status kda_kcp_apply(const float* M, float* X, const float* add, int H, int d, int n, void* stream) {
+    if (H < 0 || d < 1 || d > 256 || n < 1) return KDA_ERR_SHAPE;
+    if (H > 0 && (!M || !X)) return KDA_ERR_NULL;
+    if (misaligned(M) || misaligned(X) || misaligned(add)) return KDA_ERR_ALIGN;
+    if (X == M || (add && X == add)) return KDA_ERR_SHAPE;
+    cudaError_t e = kda::launch_kcp_apply(M, X, add, H, d, n, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KDA_OK : cuda_fail(e);
 }
 

@@ -91,8 +91,10 @@ prefill_recurrent_kernel(kda_prefill_args a) {
             const float u = a.beta[tok] * (s_v[tid] - w);
             s_u[tid] = u;
             o_e = a.scale * (qs + kqn * u);
-            if (BF16) reinterpret_cast<uint16_t*>(a.o)[tok * D + tid] = f_to_bf16(o_e);
-            else reinterpret_cast<float*>(a.o)[tok * D + tid] = o_e;
+            if (a.o) {
+                if (BF16) reinterpret_cast<uint16_t*>(a.o)[tok * D + tid] = f_to_bf16(o_e);
+                else reinterpret_cast<float*>(a.o)[tok * D + tid] = o_e;
+            }
         }
         float ss = warp_sum(o_e * o_e);
         if (lane == 0) s_red[3][warp] = ss;

@@ -897,7 +897,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         tc::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < HW; ++c) o[c] *= a.scale;
-        if (t < nco) {
+        if (t < nco && a.o) {
             uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
 #pragma unroll
             for (int c = 0; c < HW; c += 8) store8_bf16(dst + c, o + c);
@@ -975,7 +975,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         // the next record into the other TMEM buffers, the one after it into registers
         if (j > 0) {
             if (gate) cluster_wait();
-            if (row >= C) emit_outputs(j - 1);
+            if (row >= C && (a.o || gate)) emit_outputs(j - 1);
         }
         if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
         if (j + 2 < nch) load_rec(j + 2);
@@ -1084,7 +1084,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     // outputs of the last chunk
     if (nch > 0) {
         if (gate) cluster_wait();
-        if (row >= C) emit_outputs(nch - 1);
+        if (row >= C && (a.o || gate)) emit_outputs(nch - 1);
     }
 
     // ---- final state

@@ -648,7 +648,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
 #pragma unroll
                     for (int j = 0; j < 16; ++j) { o[c + j] = a.scale * v[j]; ss += o[c + j] * o[c + j]; }
                 }
-                if (t < nc) {
+                if (t < nc && a.o) {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0 + t) * H + h) * D + NE * r + c_lo;
 #pragma unroll
                     for (int c = 0; c < NE / 2; c += 8) store8_bf16(dst + c, o + c);

@@ -24,7 +24,7 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
             "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count",
-            "kda_short_conv", "kda_short_conv_step"]
+            "kda_short_conv", "kda_short_conv_step", "kda_kcp_apply"]
 
 _vp = ctypes.c_void_p
 
@@ -105,6 +105,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_prefill_snapshot_count.argtypes = [ctypes.POINTER(PrefillArgs)]
     lib.kda_prefill_snapshot_count.restype = ctypes.c_long
     lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+    lib.kda_kcp_apply.restype = ctypes.c_int
+    lib.kda_kcp_apply.argtypes = [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp]
     lib.kda_short_conv.restype = ctypes.c_int
     lib.kda_short_conv.argtypes = [ctypes.POINTER(ShortConvArgs), _vp]
     lib.kda_short_conv_step.restype = ctypes.c_int
@@ -199,6 +201,7 @@ def prefill_raw(args: PrefillArgs, stream=None, recurrent: bool = False):
 
 
 PREFILL_MIN_WORKSPACE = 256   # smallest workspace of the tensor-core path (single-pass schedule)
+_WS_CACHE = {}                # prefill(workspace="cache"): one buffer per device
 
 
 def snapshot_count(cu_seqlens_host, interval: int) -> int:
@@ -209,7 +212,8 @@ def snapshot_count(cu_seqlens_host, interval: int) -> int:
 
 def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=None,
             g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, want_state=True,
-            out=None, stream=None, recurrent=False, workspace=None, snap_interval=0, gate="bounded"):
+            out=None, stream=None, recurrent=False, workspace=None, snap_interval=0, gate="bounded",
+            want_o=True):
     """KDA chunked prefill through ``kda_prefill``.
 
     q, k, z: [T, H, dk]; v: [T, H, dv]; beta: [T, H]; A: [H]; cu_seqlens: int32
@@ -223,7 +227,7 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
         cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
     cu_host = cu_seqlens.to("cpu")
     N = cu_host.numel() - 1
-    o = out["o"] if out else torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    o = (out["o"] if out else torch.empty((T, H, dv), dtype=q.dtype, device=dev)) if want_o else None
     S_T = (out["S_T"] if out else torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)) \
         if want_state else None
     y = None
@@ -243,8 +247,15 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
         need = prefill_workspace_size(args)
         if need > 0:
             # a caller's workspace is used as given: its size picks the schedule
-            # (>= need: chunk-parallel; >= PREFILL_MIN_WORKSPACE: single pass)
-            if workspace is None:
+            # (>= need: chunk-parallel; >= PREFILL_MIN_WORKSPACE: single pass);
+            # "cache" reuses one buffer per device, grown on demand
+            if isinstance(workspace, str) and workspace == "cache":
+                key = (dev.type, dev.index)
+                ws = _WS_CACHE.get(key)
+                if ws is None or ws.numel() < need:
+                    _WS_CACHE[key] = ws = torch.empty(need, dtype=torch.uint8, device=dev)
+                workspace = ws
+            elif workspace is None:
                 workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
             args.workspace = workspace.data_ptr()
             args.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -347,6 +358,15 @@ def short_conv_step(x, weight, state, bias=None, slots=None, activation=True, st
     a.activation = int(bool(activation))
     _check(load_library().kda_short_conv_step(ctypes.byref(a), _stream(stream)), "kda_short_conv_step")
     return y
+
+
+def kcp_apply(M, X, add=None, stream=None):
+    """X[h] <- M[h] X[h] + add[h] for every head, in place (``kda_kcp_apply``).
+    M [H, d, d], X [H, d, n], add [H, d, n] or None; float32 on the device."""
+    H, d, n = X.shape
+    _check(load_library().kda_kcp_apply(_p(M), _p(X), _p(add), int(H), int(d), int(n), _stream(stream)),
+           "kda_kcp_apply")
+    return X
 
 
 def gate_norm(o, g_in, norm_w=None, eps=1e-6, out=None, stream=None):

@@ -1,0 +1,102 @@
+"""KDA context parallelism (Sec. 10.2) on the GPU: the transition pair of a
+segment from two state-only prefills, kda_kcp_apply, and the one-device KCP
+driver (ranks taken in turn) against the single-pass prefill and the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import chunked
+from serving_kda_chunked_gated_gb300 import inputs as I
+from kda_testutil import TOL_O, TOL_S, f64, host, qkv_to_dev, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _segments(d, dev, cuts):
+    q, k, v = qkv_to_dev(d, dev)
+    z, beta = to_dev(d["z"], dev), to_dev(d["beta"], dev)
+    A = to_dev(d["A"], dev)
+    segs = []
+    for i in range(len(cuts) - 1):
+        sl = slice(cuts[i], cuts[i + 1])
+        segs.append(dict(q=q[sl].clone(), k=k[sl].clone(), v=v[sl].clone(), z=z[sl].clone(), beta=beta[sl].clone(),
+                         A=A))
+    return segs
+
+
+def test_pair_from_state_only_prefills(kda_lib, cuda_dev):
+    """M of a short, weakly decaying segment (over long segments of the workload's
+    decays M underflows fp32: the pairs' M carries no memory there)."""
+    from serving_kda_chunked_gated_gb300 import kcp
+    d = I.make_prefill(I.workload("prefill_128k", T=100, H=2))
+    d["z"] = (d["z"] - 4.0).astype(np.float32)
+    seg = _segments(d, cuda_dev, [0, 100])[0]
+    M, St = kcp.GpuOps().pair(seg)
+    torch.cuda.synchronize()
+    qn = f64(d, "q")
+    kn = f64(d, "k")
+    kn = kn / np.sqrt((kn * kn).sum(-1, keepdims=True) + 1e-6)   # the prefill's L2Norm of k
+    for h in range(2):
+        g = oracle.log_decay(d["z"][:, h], d["A"][h])
+        rM, rSt = chunked.kcp_pair(kn[:, h], f64(d, "v")[:, h], g, d["beta"][:, h].astype(np.float64))
+        assert rel(host(M[h]), rM) < TOL_S and rel(host(St[h]), rSt) < TOL_S
+
+
+@pytest.mark.parametrize("n", [128, 256, 40])
+def test_kcp_apply(kda_lib, cuda_dev, n):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    g = torch.Generator().manual_seed(n)
+    H, dd = 3, 128
+    M = torch.randn((H, dd, dd), generator=g) / 12
+    X = torch.randn((H, dd, n), generator=g)
+    add = torch.randn((H, dd, n), generator=g)
+    ref = torch.matmul(M.double(), X.double()) + add.double()
+    Xd = X.to(cuda_dev)
+    kda.kcp_apply(M.to(cuda_dev), Xd, add.to(cuda_dev))
+    torch.cuda.synchronize()
+    assert rel(Xd.cpu().numpy(), ref.numpy()) < 1e-6
+    X2 = X.to(cuda_dev)
+    kda.kcp_apply(M.to(cuda_dev), X2)
+    torch.cuda.synchronize()
+    assert rel(X2.cpu().numpy(), torch.matmul(M.double(), X.double()).numpy()) < 1e-6
+
+
+def test_local_kcp_matches_single_pass_and_oracle(kda_lib, cuda_dev):
+    import serving_kda_chunked_gated_gb300.kda as kda
+    from serving_kda_chunked_gated_gb300 import kcp
+    T, cuts = 1000, [0, 250, 251, 700, 1000]
+    d = I.make_prefill(I.workload("prefill_128k", T=T, H=2))
+    segs = _segments(d, cuda_dev, cuts)
+    outs = kcp.kcp_prefill_local(segs, kcp.GpuOps())
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    o1, S1, _ = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev))
+    torch.cuda.synchronize()
+    o = torch.cat([x[0] for x in outs])
+    assert rel(host(o), host(o1)) < TOL_O and rel(host(outs[-1][1]), host(S1[0])) < TOL_S
+    ro, rS, _ = oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"])
+    assert rel(host(o), ro) < TOL_O and rel(host(outs[-1][1]), rS[0]) < TOL_S
+
+
+def test_local_kcp_full_size_eight_segments(kda_lib, cuda_dev):
+    """131072 tokens x 32 heads in eight 16384-token segments: the KCP result
+    equals the single-pass prefill, and one head equals the oracle."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    from serving_kda_chunked_gated_gb300 import kcp
+    w = I.workload("prefill_128k")
+    d = I.make_prefill(w)
+    T = d["q"].shape[0]
+    cuts = list(range(0, T + 1, T // 8))
+    segs = _segments(d, cuda_dev, cuts)
+    outs = kcp.kcp_prefill_local(segs, kcp.GpuOps())
+    o = torch.cat([x[0] for x in outs])
+    S_kcp = outs[-1][1]
+    del segs, outs
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    o1, S1, _ = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev))
+    torch.cuda.synchronize()
+    assert rel(host(o), host(o1)) < TOL_O and rel(host(S_kcp), host(S1[0])) < TOL_S
+    heads = [9]
+    ds = I.make_prefill(w, heads=heads)
+    ro, rS, _ = oracle.prefill(f64(ds, "q"), f64(ds, "k"), f64(ds, "v"), ds["z"], ds["beta"], ds["A"])
+    assert rel(host(o[:, heads]), ro) < TOL_O and rel(host(S_kcp[heads]), rS[0]) < TOL_S
