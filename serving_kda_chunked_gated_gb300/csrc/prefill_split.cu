@@ -289,27 +289,29 @@ prep_kernel(kda_prefill_args a, Work w,
         wait(bar_in, ph_in);
         ph_in ^= 1u;
 
-        // ---- 1a. q/k L2 norms (warp w: tokens 8w..8w+7)
-#pragma unroll 4
-        for (int i = 0; i < 8; ++i) {
-            const int t = warp * 8 + i;
-            float sq = 0.f, sk = 0.f;
+        // ---- 1a. q/k L2 norms: threads 2v and 2v+1 cover vector v (q of token v for
+        //          v < 64, else k of token v - 64), 64 dims each, reading 16-byte chunks in
+        //          a rotated order so that each quarter-warp hits 8 distinct bank groups
+        {
+            const int v = tid >> 1, half = tid & 1;
+            const int t = v & (C - 1);
+            const uint16_t* rowp = (v < C ? sRawQ : sRawK) + t * D + half * (D / 2);
+            float ssum = 0.f;
             if (t < nc) {
-                const uint2 qa = *reinterpret_cast<const uint2*>(sRawQ + t * D + 4 * lane);
-                const uint2 ka = *reinterpret_cast<const uint2*>(sRawK + t * D + 4 * lane);
-                const float q0 = __uint_as_float(qa.x << 16), q1 = __uint_as_float(qa.x & 0xffff0000u),
-                            q2 = __uint_as_float(qa.y << 16), q3 = __uint_as_float(qa.y & 0xffff0000u);
-                const float k0 = __uint_as_float(ka.x << 16), k1 = __uint_as_float(ka.x & 0xffff0000u),
-                            k2 = __uint_as_float(ka.y << 16), k3 = __uint_as_float(ka.y & 0xffff0000u);
-                sq = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
-                sk = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = (i + 2 * v + half) & 7;
+                    const uint4 u = *reinterpret_cast<const uint4*>(rowp + 8 * c);
+                    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float lo = __uint_as_float(wv[j] << 16), hi = __uint_as_float(wv[j] & 0xffff0000u);
+                        ssum = fmaf(lo, lo, fmaf(hi, hi, ssum));
+                    }
+                }
             }
-            sq = warp_sum(sq);
-            sk = warp_sum(sk);
-            if (lane == 0) {
-                s_rq[t] = a.qk_l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
-                s_rk[t] = a.qk_l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
-            }
+            ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+            if (half == 0) (v < C ? s_rq : s_rk)[t] = a.qk_l2norm ? rsqrtf(ssum + 1e-6f) : 1.f;
         }
         __syncthreads();
 
