@@ -192,6 +192,7 @@ static_assert(3 * C * AS * 4 + (NT / 32) * 16 * 16 * 4 <= RB_BYTES, "region RB h
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;
 constexpr uint32_t BYTES_V = C * D * 2;
+constexpr int NTP = 512;         // threads per CTA (16 warps; warps w, w+4, w+8, w+12 share TMEM lanes)
 constexpr uint32_t TM_D = 0;     // 256 cols: [U | W ; U_o | P Gamma K]
 constexpr uint32_t TM_A2 = 256;  // 64 cols: [T beta ; P beta]
 constexpr uint32_t TM_COLS = 512;
@@ -200,7 +201,7 @@ constexpr uint32_t TM_COLS = 512;
 // GATE 0: K3's bounded gate; 1: Kimi Linear's Softplus gate, whose diagonal Gram
 // sub-blocks are formed pair by pair (their sub-chunk factors can exceed fp32)
 template <int GATE>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(prep::NTP, 1)
 prep_kernel(kda_prefill_args a, Work w,
             const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v) {
@@ -234,9 +235,8 @@ prep_kernel(kda_prefill_args a, Work w,
 
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, hf = warp >> 2;
+    const int quad = warp & 3, grp = warp >> 2;   // TMEM lane quarter, column quarter
     const int row = quad * 32 + lane;
-    const int c_lo = hf * 32;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const long stride = gridDim.x;
     long rec = blockIdx.x;
@@ -292,7 +292,7 @@ prep_kernel(kda_prefill_args a, Work w,
         // ---- 1a. q/k L2 norms: threads 2v and 2v+1 cover vector v (q of token v for
         //          v < 64, else k of token v - 64), 64 dims each, reading 16-byte chunks in
         //          a rotated order so that each quarter-warp hits 8 distinct bank groups
-        {
+        if (tid < 2 * D) {
             const int v = tid >> 1, half = tid & 1;
             const int t = v & (C - 1);
             const uint16_t* rowp = (v < C ? sRawQ : sRawK) + t * D + half * (D / 2);
@@ -315,11 +315,11 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
 
-        // ---- 1b. gate and sub-chunk-relative decay factors (channel d, sub-chunks 2hf, 2hf+1)
+        // ---- 1b. gate and sub-chunk-relative decay factors (thread: channel d, sub-chunk b)
         {
             const int d = tid & (D - 1);
 #pragma unroll 1
-            for (int b = 2 * (tid >> 7); b < 2 * (tid >> 7) + 2; ++b) {
+            for (int b = tid >> 7; b < (tid >> 7) + 1; ++b) {   // channel d, sub-chunk b
                 float al[16], kv[16], qv[16], Lc[16];
                 float F1 = 1.f, L = 0.f;
 #pragma unroll
@@ -406,36 +406,36 @@ prep_kernel(kda_prefill_args a, Work w,
         __syncthreads();
 
         // ---- 2. Gram sub-blocks, mma.sync tf32: blocks 0..9 of A_qk, 10..19 of A_kk.
-        //         Warp w forms blocks w and w+8 whole and one K-half (w & 1) of block
-        //         16 + w/2; the two halves of blocks 16..19 are added in a fixed order.
+        //         Warp w forms block w whole and one K-quarter (w & 3) of block 16 + w/4;
+        //         the four quarters of blocks 16..19 are added in a fixed order.
         {
             const int g = lane >> 2, t4 = lane & 3;
-            float* part = sAkk + C * AS;               // [8 warps][16][16] half-block partials
-            float acc[3][2][4];
+            float* part = sAkk + C * AS;               // [16 warps][16][16] quarter-block partials
+            float acc[2][2][4];
 #pragma unroll
-            for (int it = 0; it < 3; ++it)
+            for (int it = 0; it < 2; ++it)
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh)
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
-            int ia[3], ib[3];
-            bool kk[3];
+            int ia[2], ib[2];
+            bool kk[2];
 #pragma unroll
-            for (int it = 0; it < 3; ++it) {
-                const int blk_id = it < 2 ? warp + 8 * it : 16 + (warp >> 1);
+            for (int it = 0; it < 2; ++it) {
+                const int blk_id = it == 0 ? warp : 16 + (warp >> 2);
                 kk[it] = blk_id >= NPAIR;
                 const int pr = kk[it] ? blk_id - NPAIR : blk_id;
                 const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
                 ia[it] = aa;
                 ib[it] = pr - aa * (aa + 1) / 2;
             }
-            const int khalf = warp & 1;
+            const int kq = warp & 3;
 #pragma unroll 2
             for (int ks = 0; ks < 16; ++ks) {
                 const int k0 = 8 * ks + t4, k1 = k0 + 4;
 #pragma unroll
-                for (int it = 0; it < 3; ++it) {
-                    if ((it < 2 || (ks >> 3) == khalf) && !(GATE && ia[it] == ib[it])) {
+                for (int it = 0; it < 2; ++it) {
+                    if ((it == 0 || (ks >> 2) == kq) && !(GATE && ia[it] == ib[it])) {
                         const float* Arows = kk[it] ? sKr : sQ;
                         const int ra = 16 * ia[it] + g;
                         const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
@@ -452,7 +452,7 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
             }
 #pragma unroll
-            for (int it = 0; it < 3; ++it) {
+            for (int it = 0; it < 2; ++it) {
                 float* Out = kk[it] ? sAkk : sAqk;
 #pragma unroll
                 for (int nh = 0; nh < 2; ++nh) {
@@ -462,7 +462,7 @@ prep_kernel(kda_prefill_args a, Work w,
                         const int J = 16 * ib[it] + 8 * nh + 2 * t4;
                         float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
                         if (GATE && ia[it] == ib[it]) continue;   // formed pair by pair
-                        if (it == 2) {   // raw half-block partial
+                        if (it == 1) {   // raw quarter-block partial
                             *reinterpret_cast<float2*>(part + warp * 256 + (g + 8 * hr) * 16 + 8 * nh + 2 * t4) =
                                 make_float2(v0, v1);
                             continue;
@@ -480,7 +480,7 @@ prep_kernel(kda_prefill_args a, Work w,
             __syncthreads();
             if (GATE) {   // diagonal blocks from the pair-by-pair sums: 2 x 4 blocks of 16 x 16
 #pragma unroll 1
-                for (int x = tid; x < 2 * 4 * 256; x += NT) {
+                for (int x = tid; x < 2 * 4 * 256; x += NTP) {
                     const int kkb = x >> 10, bb = (x >> 8) & 3, i = (x >> 4) & 15, j = x & 15;
                     float val = 0.f;
                     if (j <= i && (j < i || !kkb)) {
@@ -492,17 +492,20 @@ prep_kernel(kda_prefill_args a, Work w,
                     (kkb ? sAkk : sAqk)[(16 * bb + i) * AS + 16 * bb + j] = val;
                 }
             }
-            if (!GATE || (tid >> 6) < 3) {   // blocks 16..19 = A_kk pairs (3, q): halves from warps 2q, 2q+1
+            if (tid < 256 && (!GATE || (tid >> 6) < 3)) {   // blocks 16..19 = A_kk pairs (3, q)
                 const int q = tid >> 6, e = (tid & 63) * 4;
                 const int I = 48 + (e >> 4), J = 16 * q + (e & 15);
-                const float4 h0 = *reinterpret_cast<const float4*>(part + (2 * q) * 256 + e);
-                const float4 h1 = *reinterpret_cast<const float4*>(part + (2 * q + 1) * 256 + e);
+                const float* pq = part + (4 * q) * 256 + e;   // quarters from warps 4q .. 4q+3
+                const float4 h0 = *reinterpret_cast<const float4*>(pq);
+                const float4 h1 = *reinterpret_cast<const float4*>(pq + 256);
+                const float4 h2 = *reinterpret_cast<const float4*>(pq + 512);
+                const float4 h3 = *reinterpret_cast<const float4*>(pq + 768);
                 const float bI = s_beta[I];
                 float4 o;
-                o.x = (J >= I) ? 0.f : (h0.x + h1.x) * bI;
-                o.y = (J + 1 >= I) ? 0.f : (h0.y + h1.y) * bI;
-                o.z = (J + 2 >= I) ? 0.f : (h0.z + h1.z) * bI;
-                o.w = (J + 3 >= I) ? 0.f : (h0.w + h1.w) * bI;
+                o.x = (J >= I) ? 0.f : ((h0.x + h1.x) + (h2.x + h3.x)) * bI;
+                o.y = (J + 1 >= I) ? 0.f : ((h0.y + h1.y) + (h2.y + h3.y)) * bI;
+                o.z = (J + 2 >= I) ? 0.f : ((h0.z + h1.z) + (h2.z + h3.z)) * bI;
+                o.w = (J + 3 >= I) ? 0.f : ((h0.w + h1.w) + (h2.w + h3.w)) * bI;
                 *reinterpret_cast<float4*>(sAkk + I * AS + J) = o;
             }
         }
@@ -607,7 +610,8 @@ prep_kernel(kda_prefill_args a, Work w,
             const float* src = (row < C ? sT : sAqk) + i * AS;
             float v[16];
 #pragma unroll
-            for (int c = c_lo; c < c_lo + C / 2; c += 16) {
+            {
+                const int c = 16 * grp;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int col = c + j;
@@ -622,11 +626,12 @@ prep_kernel(kda_prefill_args a, Work w,
 
         // ---- 4. B_pre = [V | Gamma K]^T (256 rows), the record's (K gamma_C/Gamma)^T and gamma_C
         {
-            if (tid < D) {                       // rows 0..127: value columns
-                const int e = tid;
+            const int rr = tid & (2 * D - 1), th = tid >> 8;   // B_pre row, half of the tokens
+            if (rr < D) {                        // rows 0..127: value columns
+                const int e = rr;
                 const uint8_t* vt = sRawV + (e >> 6) * (C * 128);
 #pragma unroll 4
-                for (int t = 0; t < C; t += 4) {
+                for (int t = 32 * th; t < 32 * th + 32; t += 4) {
                     float4 w4;
                     float* wp = &w4.x;
 #pragma unroll
@@ -635,11 +640,11 @@ prep_kernel(kda_prefill_args a, Work w,
                                              : 0.f;
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, 2 * D)) = w4;
                 }
-                w.gm[rec * GM_FLOATS + e] = s_gam[e];
+                if (th == 0) w.gm[rec * GM_FLOATS + e] = s_gam[e];
             } else {                             // rows 128..255: (Gamma K)^T
-                const int d = tid - D;
+                const int d = rr - D;
 #pragma unroll 4
-                for (int t = 0; t < C; t += 4) {
+                for (int t = 32 * th; t < 32 * th + 32; t += 4) {
                     float4 w4;
                     float* wp = &w4.x;
                     const float es = s_expS[(t >> 4) * D + d];
@@ -648,14 +653,14 @@ prep_kernel(kda_prefill_args a, Work w,
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(D + d, t, 2 * D)) = w4;
                 }
             }
-            const int d = row;                   // (K gamma_C / Gamma)^T: row d, 32 token columns
-            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + c_lo;
+            const int d = row;                   // (K gamma_C / Gamma)^T: row d, sub-chunk grp (16 tokens)
+            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + 16 * grp;
+            const float ec = s_expCE[grp * D + d];
 #pragma unroll
-            for (int t = 0; t < C / 2; t += 8) {
-                const float ec = s_expCE[((c_lo + t) >> 4) * D + d];
+            for (int t = 0; t < 16; t += 8) {
                 float k8[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(sK[(c_lo + t + u) * QS + d] * ec);
+                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(sK[(16 * grp + t + u) * QS + d] * ec);
                 st_stream_f8(dst + t, k8);
             }
             tc::tmem_st_wait();
@@ -693,22 +698,22 @@ prep_kernel(kda_prefill_args a, Work w,
             tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, nxt.h * D, nxt.t0, bar_in);
         }
 
-        // ---- 6. the record: [U ; U_o] and [-W ; Gamma Q - P Gamma K] (row = lane, 64 columns)
+        // ---- 6. the record: [U ; U_o] and [-W ; Gamma Q - P Gamma K] (row = lane, 32 columns)
         {
             float v[16];
-            float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 64 * hf;
-            float* aw = w.aw + rec * AW_FLOATS + (size_t)row * D + 64 * hf;
-#pragma unroll 1
-            for (int c = 0; c < 64; c += 16) {
-                tc::tmem_ld16(T0 + TM_D + lane_base + 64 * hf + c, v);
+            float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 32 * grp;
+            float* aw = w.aw + rec * AW_FLOATS + (size_t)row * D + 32 * grp;
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
                 tc::tmem_ld_wait();
                 st_stream_f8(uu + c, v);
                 st_stream_f8(uu + c + 8, v + 8);
             }
             if (row < C) {
-#pragma unroll 1
-                for (int c = 0; c < 64; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 64 * hf + c, v);
+#pragma unroll
+                for (int c = 0; c < 32; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(-v[j]);
@@ -718,14 +723,14 @@ prep_kernel(kda_prefill_args a, Work w,
             } else {
                 const int t = row - C;
                 const float* es = s_expS + (t >> 4) * D;
-#pragma unroll 1
-                for (int c = 0; c < 64; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 64 * hf + c, v);
+#pragma unroll
+                for (int c = 0; c < 32; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
                     tc::tmem_ld_wait();
                     float o4[16];
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
-                        const int d = 64 * hf + c + j;
+                        const int d = 32 * grp + c + j;
                         const float4 q4 = *reinterpret_cast<const float4*>(sQ + t * QS + d);
                         const float4 e4 = *reinterpret_cast<const float4*>(es + d);
                         o4[j] = tc::to_tf32(q4.x * e4.x - v[j]);
@@ -1203,9 +1208,9 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
         const int nsm = spl::sm_count();
         const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
         if (a.gate_mode == KDA_GATE_SOFTPLUS)
-            spl::prep_kernel<1><<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            spl::prep_kernel<1><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
         else
-            spl::prep_kernel<0><<<(unsigned)grid, spl::NT, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            spl::prep_kernel<0><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
         ++launched;
     }
     dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
