@@ -247,3 +247,21 @@ def test_options_scale_norm_weight_no_l2norm(kda_lib, cuda_dev):
     assert rel(host(o), ro) < TOL_O
     assert rel(host(y), ry) < TOL_O
     assert rel(host(S_T), rS) < TOL_S
+
+
+@pytest.mark.parametrize("T,slab", [(1000, 256), (300, 4096), (12345, 2048)])
+def test_prefill_from_host_pipelined(kda_lib, cuda_dev, T, slab):
+    """The slab-pipelined host-buffer prefill equals the one-shot device call bit
+    for bit (slabs end on chunk boundaries; the state carries in FP32)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    d = I.make_prefill(I.workload("prefill_128k", T=T, H=2))
+    pin = lambda x, bf: (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16) if bf
+                         else torch.from_numpy(np.ascontiguousarray(x))).pin_memory()
+    hq, hk, hv, hg = (pin(d[n], True) for n in ("q", "k", "v", "g_in"))
+    hz, hb, hA, hS0 = (pin(d[n], False) for n in ("z", "beta", "A", "S0"))
+    o_h, S_h, y_h = kda.prefill_from_host(hq, hk, hv, hz, hb, hA, S0=hS0, g_in=hg, slab=slab)
+    torch.cuda.synchronize()
+    o, S_T, y = kda.prefill(hq.to(cuda_dev), hk.to(cuda_dev), hv.to(cuda_dev), hz.to(cuda_dev), hb.to(cuda_dev),
+                            hA.to(cuda_dev), S0=hS0.to(cuda_dev), g_in=hg.to(cuda_dev))
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o.cpu()) and torch.equal(y_h, y.cpu()) and torch.equal(S_h, S_T.cpu())
