@@ -68,8 +68,10 @@ KDA_DEV void load8_bf16(const uint16_t* p, float* out) {
 KDA_DEV void store8_bf16(uint16_t* p, const float* in) {
     uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        w[i] = (uint32_t)f_to_bf16(in[2 * i]) | ((uint32_t)f_to_bf16(in[2 * i + 1]) << 16);
+    for (int i = 0; i < 4; ++i) {   // one round-to-nearest-even conversion per pair, in[2i] in the low half
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
     *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 

@@ -771,9 +771,11 @@ struct ScanCfg {
     static constexpr int OFF_G0 = OFF_VOP + NE * C * 4;
     static constexpr int OFF_G1 = OFF_G0 + G_TILE;
     static constexpr int OFF_SMALL = OFF_G1 + G_TILE;
-    // small region (floats): peers' row sums [2 parity][R source][C], own halves [2][2][C]
-    static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_FLOATS = SM_ROWPART + 4 * C;
-    static constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
+    // small region (floats): peers' row sums [2 parity][R source][C], own halves [2][2][C],
+    // RMSNorm weights of this CTA's columns [NE]
+    static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_NORMW = SM_ROWPART + 4 * C;
+    static constexpr int SM_FLOATS = SM_NORMW + NE;
+    static constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 256 + 1024;
     static constexpr uint32_t TM_D = 0;                      // 2 x NE cols: [U ; U_o] -> [V' ; O]
     static constexpr uint32_t TM_A3 = 2 * NE;                // 2 x 64 cols: (K gamma_C / Gamma)^T
     static constexpr uint32_t TM_DS = TM_A3 + 2 * C;         // NE cols: state increment
@@ -784,9 +786,27 @@ struct ScanCfg {
     static_assert(TM_S + NE <= TM_COLS, "TMEM budget");
 };
 
-TC_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-TC_DEV void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory"); }
-TC_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// 4-byte store into a peer CTA's shared memory that completes 4 transaction bytes
+// on the peer's mbarrier (no fence: the mbarrier phase carries the data)
+TC_DEV void st_async_f32(uint32_t addr, float v, uint32_t mbar_addr) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(addr), "r"(__float_as_uint(v)), "r"(mbar_addr) : "memory");
+}
+// arrive on a peer CTA's mbarrier; release at CTA scope orders this CTA's earlier
+// shared-memory reads (gathered by a __syncthreads) before the peer's refill, and
+// unlike a cluster-scope release it does not wait for the thread's global traffic
+TC_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+TC_DEV bool mbar_try_wait_cluster(uint64_t* mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(tc::smem_u32(mbar)), "r"(parity) : "memory");
+    return ok != 0;
+}
 
 // byte offset of bf16 element (row, col) in a g_in tile of NE columns: the 128-byte
 // rows of NE = 64 come swizzled by TMA, narrower rows are plain
@@ -816,10 +836,13 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     float* fs = reinterpret_cast<float*>(sm + Cfg::OFF_SMALL);
     float* s_rowsq = fs + Cfg::SM_ROWSQ;      // [2][R][C] peers' row sums, by parity and source
     float* s_rowpart = fs + Cfg::SM_ROWPART;  // [2][2][C] this CTA's, by parity and column half
+    float* s_normw = fs + Cfg::SM_NORMW;      // [NE] RMSNorm weights (ones without norm_w)
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + Cfg::SM_FLOATS);
     uint64_t* bar_aw = mbar + 1;         // [2]
     uint64_t* bar_g = mbar + 3;          // [2]
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 5);
+    uint64_t* bar_full = mbar + 5;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
+    uint64_t* bar_free = mbar + 7;       // [2][R] peer p has read this CTA's row sums of chunk j
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 7 + 2 * R);
 
     const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
@@ -839,9 +862,15 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     auto g_buf = [&](int b) { return sm + (b ? Cfg::OFF_G1 : Cfg::OFF_G0); };
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
+    if (tid < NE) s_normw[tid] = a.norm_w ? a.norm_w[NE * r + tid] : 1.f;
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
-        for (int b = 0; b < 2; ++b) { tc::mbar_init(bar_aw + b, 1); tc::mbar_init(bar_g + b, 1); }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(bar_aw + b, 1);
+            tc::mbar_init(bar_g + b, 1);
+            tc::mbar_init(bar_full + b, 1);
+            for (int p = 0; p < R; ++p) tc::mbar_init(bar_free + b * R + p, 1);
+        }
         tc::mbar_fence_init();
         tc::tma_prefetch_desc(&tm_aw);
         if (gate) tc::tma_prefetch_desc(&tm_g);
@@ -865,6 +894,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     // keeps its cluster barriers, so the peer CTAs are never left waiting)
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
+    };
+    auto wait_cl = [&](uint64_t* bar, uint32_t parity) {
+        for (uint32_t i = 0; !timed_out && !mbar_try_wait_cluster(bar, parity); )
+            if (++i == (1u << 22)) timed_out = true;
     };
     auto mma_wait = [&]() {
         wait(mbar, ph_mma);
@@ -911,6 +944,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         }
         if (gate) {
             wait(bar_g + bo, (jo >> 1) & 1);
+            wait_cl(bar_full + bo, (jo >> 1) & 1);
             if (t < nco) {
                 const uint8_t* sG = g_buf(bo);
                 float tot = s_rowpart[(bo * 2) * C + t] + s_rowpart[(bo * 2 + 1) * C + t];
@@ -923,12 +957,14 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int c = 0; c < HW; c += 8) {
                     const uint4 g8 = *reinterpret_cast<const uint4*>(sG + gtile_offset<NE>(t, c_lo + c));
                     const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                    const float4 wa = reinterpret_cast<const float4*>(s_normw + c_lo + c)[0];
+                    const float4 wb = reinterpret_cast<const float4*>(s_normw + c_lo + c)[1];
+                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
                     float yv[8];
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) {
                         const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
-                        const float wn = a.norm_w ? a.norm_w[NE * r + c_lo + c + jj] : 1.f;
-                        yv[jj] = sigmoidf_fast(gv) * wn * o[c + jj] * rr;
+                        yv[jj] = __fdividef(o[c + jj] * wv[jj] * rr, 1.0f + __expf(-gv));
                     }
                     store8_bf16(yp + c, yv);
                 }
@@ -958,6 +994,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     }
     tc::fence_before_sync();
     __syncthreads();
+    if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
 
 #pragma unroll 1
     for (int j = 0; j < nch; ++j) {
@@ -977,13 +1014,13 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
                                 tc::idesc_tf32(128, NE), 1);
             tc::mma_commit(mbar);
+            // the peers' row sums of this chunk (phase j - 2 of this barrier completed
+            // before the previous chunk's closing __syncthreads)
+            if (gate) tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4);
         }
         // while it runs: outputs of the previous chunk (their buffer is refilled next),
         // the next record into the other TMEM buffers, the one after it into registers
-        if (j > 0) {
-            if (gate) cluster_wait();
-            if (row >= C && (a.o || gate)) emit_outputs(j - 1);
-        }
+        if (j > 0 && row >= C && (a.o || gate)) emit_outputs(j - 1);
         if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
         if (j + 2 < nch) load_rec(j + 2);
         tc::tmem_st_wait();
@@ -1039,17 +1076,27 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::tma_load_2d(g_buf(b ^ 1), &tm_g, h * D + NE * r, t_begin + C * (j + 1), bar_g + (b ^ 1));
             }
         }
-        if (gate) {   // this chunk's row sums to every peer, then arrive (waited on next chunk)
-            const bool writer = row >= C && hf == 0;
-            if (writer) {
-                const int t = row - C;
+        if (gate) {
+            // this chunk's row sums into every peer's s_rowsq[b], once every peer has
+            // read what this CTA wrote there for chunk j - 2 (one barrier per peer: a
+            // peer's signals reach it in order, different peers' need not)
+            if (row < C && hf == 1) {   // warps 4, 5: no MMA issue on their path
+                const int t = row;
+                if (j >= 2) {
+#pragma unroll
+                    for (int p = 1; p < R; ++p) wait_cl(bar_free + b * R + (r + p) % R, ((j - 2) >> 1) & 1);
+                }
                 const float own = s_rowpart[(b * 2) * C + t] + s_rowpart[(b * 2 + 1) * C + t];
 #pragma unroll
                 for (int p = 1; p < R; ++p)
-                    st_cluster_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own);
-                cluster_arrive();
-            } else {
-                cluster_arrive_relaxed();
+                    st_async_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own,
+                                 cluster_map(bar_full + b, (r + p) % R));
+            }
+            // the outputs of chunk j - 1 (read before the __syncthreads above) are out:
+            // each peer may overwrite s_rowsq[(j - 1) & 1] with its sums of chunk j + 1
+            if (tid == 32 && j >= 1 && j + 1 < nch) {
+#pragma unroll
+                for (int p = 1; p < R; ++p) mbar_arrive_remote(cluster_map(bar_free + (b ^ 1) * R + r, (r + p) % R));
             }
         }
 
@@ -1089,10 +1136,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         __syncthreads();
     }
     // outputs of the last chunk
-    if (nch > 0) {
-        if (gate) cluster_wait();
-        if (row >= C && (a.o || gate)) emit_outputs(nch - 1);
-    }
+    if (nch > 0 && row >= C && (a.o || gate)) emit_outputs(nch - 1);
 
     // ---- final state
     if (a.S_T) {
