@@ -184,7 +184,10 @@ constexpr int OFF_SMALL = OFF_RAWV + 2 * C * 64 * 2;
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
               SM_DIAG = SM_CTAB + NPAIR * D,            // [4 sub-chunks][9 batches][4 warps][32]
-              SM_FLOATS = SM_DIAG + 4 * 9 * 4 * 32;
+              SM_EA = SM_DIAG + 4 * 9 * 4 * 32,         // exp(A_h) of heads 0..EA_HEADS-1
+              SM_LOC = SM_EA + 128,                     // record walk (ints), see prep_kernel
+              SM_FLOATS = SM_LOC + 16;
+constexpr int EA_HEADS = 128;
 constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
 static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0, "swizzled tiles need 1024-B alignment");
 static_assert(2 * D * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
@@ -228,6 +231,10 @@ prep_kernel(kda_prefill_args a, Work w,
     float* s_gam = fs + SM_GAM;
     float* s_ctab = fs + SM_CTAB;
     float* s_diag = fs + SM_DIAG;
+    float* s_eA = fs + SM_EA;
+    // s_loc: [0..2] this record's {t0, nc, h}, [3..5] the next one's; [8..15] the walk
+    // at the next record: chunk g (long), head, sequence n, cb[n], cb[n+1], cu[n], cu[n+1]
+    int* s_loc = reinterpret_cast<int*>(fs + SM_LOC);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
     uint64_t* bar_in = mbar + 1;
     uint64_t* bar_v = mbar + 2;
@@ -243,6 +250,28 @@ prep_kernel(kda_prefill_args a, Work w,
     Loc cur = locate(rec, H, a.cu_seqlens, w.chunk_base, a.num_seqs);
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
+    if (tid < EA_HEADS && tid < H) s_eA[tid] = __expf(a.A[tid]);
+    // records are visited with a fixed stride: the walk advances (g, h) without a
+    // division and searches the sequence table only when it leaves a sequence
+    const long step_g = stride / H;
+    const int step_h = (int)(stride - step_g * H);
+    if (tid == NTP - 1) {
+        s_loc[0] = cur.t0; s_loc[1] = cur.nc; s_loc[2] = cur.h;
+        const long rn = rec + stride;
+        const long g = rn / H;
+        const int hn = (int)(rn - g * H);
+        int n = 0;
+        if (rn < w.nrec) {
+            int hi = a.num_seqs;
+            while (hi - n > 1) { const int mid = (n + hi) >> 1; if (w.chunk_base[mid] <= g) n = mid; else hi = mid; }
+        }
+        *reinterpret_cast<long*>(s_loc + 8) = g;
+        s_loc[10] = hn; s_loc[11] = n;
+        s_loc[12] = w.chunk_base[n]; s_loc[13] = w.chunk_base[n + 1];
+        s_loc[14] = a.cu_seqlens[n]; s_loc[15] = a.cu_seqlens[n + 1];
+        const int t0 = s_loc[14] + C * (int)(g - s_loc[12]);
+        s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hn;
+    }
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
         tc::mbar_init(bar_in, 1);
@@ -277,11 +306,11 @@ prep_kernel(kda_prefill_args a, Work w,
     if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
 
     for (; rec < w.nrec; rec += stride) {
-        const long nrec_next = rec + stride;
-        const bool has_next = nrec_next < w.nrec;
-        const Loc nxt = has_next ? locate(nrec_next, H, a.cu_seqlens, w.chunk_base, a.num_seqs) : cur;
+        const bool has_next = rec + stride < w.nrec;
+        cur = Loc{s_loc[0], s_loc[1], s_loc[2]};
+        const Loc nxt = has_next ? Loc{s_loc[3], s_loc[4], s_loc[5]} : cur;
         const int nc = cur.nc, h = cur.h;
-        const float eA = __expf(a.A[h]);
+        const float eA = h < EA_HEADS ? s_eA[h] : __expf(__ldg(a.A + h));
         if (tid < C) {
             s_beta[tid] = beta_next;
             beta_next = (has_next && tid < nxt.nc) ? a.beta[(size_t)(nxt.t0 + tid) * H + nxt.h] : 0.f;
@@ -744,8 +773,26 @@ prep_kernel(kda_prefill_args a, Work w,
             }
             tc::fence_before_sync();
         }
+        if (tid == NTP - 1 && has_next) {   // advance the walk: this record <- the next, next <- one stride on
+            s_loc[0] = s_loc[3]; s_loc[1] = s_loc[4]; s_loc[2] = s_loc[5];
+            long g = *reinterpret_cast<const long*>(s_loc + 8) + step_g;
+            int hh = s_loc[10] + step_h;
+            if (hh >= H) { hh -= H; ++g; }
+            if (rec + 2 * stride < w.nrec) {
+                if (g >= s_loc[13]) {           // past this sequence: largest n with cb[n] <= g
+                    int n = s_loc[11] + 1, hi = a.num_seqs;
+                    while (hi - n > 1) { const int mid = (n + hi) >> 1; if (w.chunk_base[mid] <= g) n = mid; else hi = mid; }
+                    s_loc[11] = n;
+                    s_loc[12] = w.chunk_base[n]; s_loc[13] = w.chunk_base[n + 1];
+                    s_loc[14] = a.cu_seqlens[n]; s_loc[15] = a.cu_seqlens[n + 1];
+                }
+                const int t0 = s_loc[14] + C * (int)(g - s_loc[12]);
+                s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hh;
+            }
+            *reinterpret_cast<long*>(s_loc + 8) = g;
+            s_loc[10] = hh;
+        }
         __syncthreads();
-        cur = nxt;
     }
     if (timed_out && w.err) atomicOr(w.err, 1);
     drain_if(timed_out);
