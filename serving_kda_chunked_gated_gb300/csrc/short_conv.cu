@@ -9,7 +9,8 @@
 // Streaming, HBM-bound: each thread owns 8 consecutive channels (one 16-byte
 // bf16 or two 16-byte f32 accesses per token, coalesced across the warp) and
 // walks a segment of SEG packed tokens with the last W-1 inputs in registers;
-// at a sequence start it reloads the window from that sequence's state.  A
+// at a sequence start it reloads the window from that sequence's state.  One
+// lane per warp prefetches the warp's row slices into L2 a few tokens ahead.  A
 // second launch writes the new states; the decode step shifts a state in place.
 #include "kda_common.cuh"
 
@@ -97,6 +98,13 @@ __global__ void __launch_bounds__(NT) short_conv_kernel(kda_short_conv_args a) {
         }
     };
     fill(t_begin);
+    // lane 0 has the warp's row slice (its 32 threads' channels, clamped at the row
+    // end) prefetched into L2 PF tokens ahead of the loads: memory parallelism
+    // without registers
+    constexpr int PF = 8;
+    const bool pf_lane = (threadIdx.x & 31) == 0;
+    const int cw0 = c0;   // lane 0: the warp's first channel
+    const uint32_t pf_bytes = (uint32_t)(min(256, C - cw0) * (BF16 ? 2 : 4));
     // one token: y from the window and x, then slide the window
     auto step = [&](int t, const float* xv) {
         float y[8];
@@ -131,6 +139,13 @@ __global__ void __launch_bounds__(NT) short_conv_kernel(kda_short_conv_args a) {
         constexpr int U = 4;
 #pragma unroll 1
         for (; t + U <= stop; t += U) {
+            if (pf_lane && t + PF + U <= t_end) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const void* pp = reinterpret_cast<const uint8_t*>(a.x) + ((size_t)(t + PF + u) * C + cw0) * (BF16 ? 2 : 4);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(pp), "r"(pf_bytes) : "memory");
+                }
+            }
             float xv[U][8];
 #pragma unroll
             for (int u = 0; u < U; ++u) load8<BF16>(a.x, (size_t)(t + u) * C + c0, xv[u]);
