@@ -472,6 +472,7 @@ def run_ours(args, rank, world):
                      "roofline": {"bound": "hbm", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9, "peak": pk["hbm"],
                                   "unit": "GB/s", "frac": pro_bytes / (pro_ms * 1e-3) / 1e9 / pk["hbm"],
                                   "algorithmic_bytes_per_launch": pro_bytes,
+                                  "traffic": kernel_traffic("short_conv.cu", "prologue"),
                                   "launch": "three kda_short_conv calls (q, k, v)"}},
         "kcp": kcp_res,
         "e2e": e2e,
