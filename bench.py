@@ -335,8 +335,9 @@ def run_ours(args, rank, world):
     del pro
 
     # ---- KDA context parallelism (secondary): one rank's work when the sequence
-    # is split over KCP_RANKS GPUs -- its transition pair (two state-only
-    # prefills), the entry state from the other ranks' pairs, then its segment
+    # is split over KCP_RANKS GPUs -- its segment's chunk records once, its
+    # transition pair (two state-only scans over them), the entry state from the
+    # other ranks' pairs, then its segment's outputs (a third scan)
     kcp_res = None
     if N == 1 and T % KCP_RANKS == 0:
         from serving_kda_chunked_gated_gb300 import kcp as kcp_mod

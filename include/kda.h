@@ -158,6 +158,35 @@ long kda_prefill_snapshot_count(const kda_prefill_args* args);
 kda_status kda_prefill(const kda_prefill_args* args, void* stream);
 
 /*
+ * The chunk-parallel prefill in its two halves, so that one set of chunk
+ * records serves several state passes over the same tokens.  KDA context
+ * parallelism ("Kimi K3" page, Sec. 10.2) runs a rank's segment three times:
+ * its transition M (from S0 = I with v = 0), its state S~ from zero, and its
+ * outputs from the entry state; the records depend only on q, k, v, z, beta,
+ * A, cu_seqlens, qk_l2norm, g_min and gate_mode, never on S0.
+ *
+ * kda_prefill_records: writes the chunk records of args' sequences into
+ *   args->workspace, which must hold kda_prefill_workspace_size(args) bytes
+ *   (else KDA_ERR_WORKSPACE).  S0, S_T, o, g_in, norm_w, y and the snapshot
+ *   fields are not read.  Inputs and their validation as for kda_prefill;
+ *   KDA_ERR_UNSUPPORTED where kda_prefill would not take the chunk-parallel
+ *   schedule (inputs other than bf16 q/k/v with d_k = d_v = 128).
+ * kda_prefill_scan: the state recurrence over the records that
+ *   kda_prefill_records wrote into args->workspace, producing o, S_T, y and
+ *   snapshots exactly as kda_prefill (bit for bit) from args->S0.  The record
+ *   inputs of args must be those of the kda_prefill_records call (the library
+ *   cannot check this); S0 and the outputs may differ from call to call.  The
+ *   workspace is only read, so any number of scans may follow one records
+ *   call, each on any stream ordered after it.  flags: 0, or KDA_SCAN_ZERO_V:
+ *   evaluate the operator with v = 0 (the records' U parts are not read; the
+ *   outputs are those of kda_prefill with a zero v).  Other flags ->
+ *   KDA_ERR_SHAPE.
+ */
+#define KDA_SCAN_ZERO_V 1
+kda_status kda_prefill_records(const kda_prefill_args* args, void* stream);
+kda_status kda_prefill_scan(const kda_prefill_args* args, int flags, void* stream);
+
+/*
  * kda_prefill for callers that cannot allocate device memory.  (Library
  * plumbing: the KDA pages have no counterpart of this entry point.)
  *

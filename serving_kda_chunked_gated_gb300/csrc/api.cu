@@ -18,6 +18,7 @@ size_t prefill_tc_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_split_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s);
+cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int scan_flags, cudaStream_t s);
 cudaError_t launch_short_conv(const kda_short_conv_args& a, cudaStream_t s);
 cudaError_t launch_kcp_apply(const float* M, float* X, const float* Add, int H, int d, int n, cudaStream_t s);
 cudaError_t launch_short_conv_step(const kda_short_conv_step_args& a, cudaStream_t s);
@@ -126,6 +127,27 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
         e = kda::launch_prefill_recurrent(*a, s);
     }
     return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+// the chunk-parallel schedule's halves: parts 1 = records, 2 = scan
+static kda_status prefill_split_part(const kda_prefill_args* a, int parts, int flags, void* stream) {
+    kda_status st = validate_prefill(a);
+    if (st != KDA_OK) return st;
+    if (flags & ~KDA_SCAN_ZERO_V) return KDA_ERR_SHAPE;
+    if (!kda::prefill_tc_supported(*a)) return KDA_ERR_UNSUPPORTED;
+    if (a->num_seqs == 0) return KDA_OK;
+    if (!a->workspace || a->workspace_bytes < kda::prefill_split_workspace_size(*a)) return KDA_ERR_WORKSPACE;
+    if (misaligned(a->workspace)) return KDA_ERR_ALIGN;
+    const cudaError_t e = kda::launch_prefill_split_parts(*a, parts, flags, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+kda_status kda_prefill_records(const kda_prefill_args* a, void* stream) {
+    return prefill_split_part(a, 1, 0, stream);
+}
+
+kda_status kda_prefill_scan(const kda_prefill_args* a, int flags, void* stream) {
+    return prefill_split_part(a, 2, flags, stream);
 }
 
 kda_status kda_prefill_noalloc(const kda_prefill_args* a, void* stream) {

@@ -62,6 +62,7 @@ struct Work {
     float* gm;
     int* err;                // bounded waits that gave up set bit 0
     long nrec;               // chunks * H
+    int zero_v;              // scan: take v as zero (the U records are not read)
 };
 
 TC_DEV uint32_t cluster_map(const void* p, uint32_t rank) {
@@ -958,16 +959,20 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     auto load_rec = [&](int j) {
         const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
         const float* k = w.kt + rec_of(j) * KT_FLOATS + (size_t)row * C + 32 * hf;
+        if (!w.zero_v) {
 #pragma unroll
-        for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
+            for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i) ld_nc_f8(k + 8 * i, pk + 8 * i);
         pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
     };
     auto store_rec = [&](int b) {
+        if (!w.zero_v) {
 #pragma unroll
-        for (int i = 0; i < HW; i += 16)
-            tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
+            for (int i = 0; i < HW; i += 16)
+                tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
+        }
 #pragma unroll
         for (int i = 0; i < 32; i += 16)
             tc::tmem_st16(T0 + Cfg::TM_A3 + C * b + lane_base + 32 * hf + i, pk + i);
@@ -1050,7 +1055,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         const int nc = min(C, t_end - c0);
         const float gm = gm_next;
 
-        // ---- MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S
+        // ---- MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S  (U = 0 under zero_v:
+        //      the first step then ignores the accumulator)
         if (tid == 0) {
             wait(bar_aw + b, (j >> 1) & 1);
             tc::fence_after_sync();
@@ -1059,7 +1065,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
                 tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
-                                tc::idesc_tf32(128, NE), 1);
+                                tc::idesc_tf32(128, NE), (ks > 0 || !w.zero_v) ? 1u : 0u);
             tc::mma_commit(mbar);
             // the peers' row sums of this chunk (phase j - 2 of this barrier completed
             // before the previous chunk's closing __syncthreads)
@@ -1248,7 +1254,8 @@ static int sm_count() {
 
 size_t prefill_split_workspace_size(const kda_prefill_args& a) { return spl::layout(a).total; }
 
-cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
+// parts: bit 0 = plan + prep (the records), bit 1 = scan; scan_flags: KDA_SCAN_*
+cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int scan_flags, cudaStream_t s) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
@@ -1274,6 +1281,7 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
     w.kt = reinterpret_cast<float*>(recs + L.kt);
     w.gm = reinterpret_cast<float*>(recs + L.gm);
     w.nrec = L.nrec;
+    w.zero_v = (scan_flags & KDA_SCAN_ZERO_V) ? 1 : 0;
 
     const uint64_t rowq = (uint64_t)a.H * spl::D;
     const uint64_t rows = (uint64_t)a.T_total;
@@ -1293,22 +1301,31 @@ cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
     if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.aw, 128, (uint64_t)L.nrec * 128, 32, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
 
-    spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base));
-    int launched = 1;
-    if (L.nrec > 0) {
-        const int nsm = spl::sm_count();
-        const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
-        if (a.gate_mode == KDA_GATE_SOFTPLUS)
-            spl::prep_kernel<1><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
-        else
-            spl::prep_kernel<0><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+    int launched = 0;
+    if (parts & 1) {
+        spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base));
+        ++launched;
+        if (L.nrec > 0) {
+            const int nsm = spl::sm_count();
+            const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
+            if (a.gate_mode == KDA_GATE_SOFTPLUS)
+                spl::prep_kernel<1><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            else
+                spl::prep_kernel<0><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            ++launched;
+        }
+    }
+    if (parts & 2) {
+        dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
+        spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg);
         ++launched;
     }
-    dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
-    spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg);
-    ++launched;
     count_launches(launched);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s) {
+    return launch_prefill_split_parts(a, 3, 0, s);
 }
 
 }  // namespace kda

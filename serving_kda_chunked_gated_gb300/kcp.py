@@ -26,17 +26,50 @@ import torch
 
 
 class GpuOps:
-    """The per-rank KCP steps on this library's kernels (device tensors)."""
+    """The per-rank KCP steps on this library's kernels (device tensors).
 
-    def __init__(self, **prefill_kw):
+    A segment's three state passes (M from S0 = I with v = 0, S~ from zero,
+    its outputs from the entry state) share one set of chunk records: with
+    bf16 q/k/v and d = 128 the records are built once (``kda_prefill_records``)
+    and each pass is a ``kda_prefill_scan`` over them, M with the zero-v flag.
+    Other inputs take three ``kda_prefill`` calls.
+    """
+
+    REC_KW = ("g_min", "qk_l2norm", "gate")
+    SCAN_KW = ("scale", "norm_eps")
+
+    def __init__(self, reuse_records=True, **prefill_kw):
         self.kw = dict(workspace="cache")
         self.kw.update(prefill_kw)
+        self.reuse = reuse_records
+        self._rec = {}   # id(seg) -> (seg, Records)
+
+    def _records(self, seg):
+        from . import kda
+        k = seg["k"]
+        if not (self.reuse and k.dtype == torch.bfloat16 and k.shape[2] == 128 and seg["v"].shape[2] == 128):
+            return None
+        hit = self._rec.get(id(seg))
+        if hit is not None and hit[0] is seg:
+            return hit[1]
+        rec = kda.prefill_records(seg["q"], k, seg["v"], seg["z"], seg["beta"], seg["A"],
+                                  **{n: self.kw[n] for n in self.REC_KW if n in self.kw})
+        self._rec[id(seg)] = (seg, rec)
+        return rec
+
+    def _scan_kw(self):
+        return {n: self.kw[n] for n in self.SCAN_KW if n in self.kw}
 
     def pair(self, seg):
         from . import kda
         k = seg["k"]
         H, dk = k.shape[1], k.shape[2]
         eye = torch.eye(dk, dtype=torch.float32, device=k.device).expand(1, H, dk, dk).contiguous()
+        rec = self._records(seg)
+        if rec is not None:
+            _, M, _ = kda.prefill_scan(rec, S0=eye, want_o=False, zero_v=True, **self._scan_kw())
+            _, St, _ = kda.prefill_scan(rec, want_o=False, **self._scan_kw())
+            return M[0], St[0]
         # M: the state after the segment from S0 = I with v = 0 (dv = dk)
         _, M, _ = kda.prefill(seg["q"], k, torch.zeros_like(seg["v"]), seg["z"], seg["beta"], seg["A"],
                               S0=eye, want_o=False, **self.kw)
@@ -51,6 +84,12 @@ class GpuOps:
 
     def prefill(self, seg, S0):
         from . import kda
+        rec = self._records(seg)
+        if rec is not None:
+            o, S_T, y = kda.prefill_scan(rec, S0=S0.unsqueeze(0).contiguous(), g_in=seg.get("g_in"),
+                                         norm_w=seg.get("norm_w"), **self._scan_kw())
+            self._rec.pop(id(seg), None)   # the segment's last pass
+            return o, S_T[0], y
         o, S_T, y = kda.prefill(seg["q"], seg["k"], seg["v"], seg["z"], seg["beta"], seg["A"],
                                 S0=S0.unsqueeze(0).contiguous(), g_in=seg.get("g_in"), norm_w=seg.get("norm_w"),
                                 **self.kw)

@@ -24,7 +24,8 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE"
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
             "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count",
-            "kda_short_conv", "kda_short_conv_step", "kda_kcp_apply"]
+            "kda_short_conv", "kda_short_conv_step", "kda_kcp_apply", "kda_prefill_records",
+            "kda_prefill_scan"]
 
 _vp = ctypes.c_void_p
 
@@ -96,6 +97,10 @@ def load_library(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
     lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill_records.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+    lib.kda_prefill_records.restype = ctypes.c_int
+    lib.kda_prefill_scan.argtypes = [ctypes.POINTER(PrefillArgs), ctypes.c_int, _vp]
+    lib.kda_prefill_scan.restype = ctypes.c_int
     lib.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
     lib.kda_prefill_noalloc.restype = ctypes.c_int
     lib.kda_prefill_recurrent.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
@@ -357,6 +362,56 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
     prefill_raw(args, stream=stream, recurrent=recurrent)
     if snap_interval:
         return o, S_T, y, S_snap
+    return o, S_T, y
+
+
+SCAN_ZERO_V = 1   # kda_prefill_scan flag: evaluate with v = 0
+
+
+class Records:
+    """Chunk records of one set of prefill inputs (``kda_prefill_records``),
+    kept with their inputs and workspace so that several ``prefill_scan``
+    calls can run the state recurrence over them from different S0."""
+
+    def __init__(self, args, keep, workspace, shape):
+        self.args, self.keep, self.workspace, self.shape = args, keep, workspace, shape
+
+
+def prefill_records(q, k, v, z, beta, A, cu_seqlens=None, g_min=-5.0, qk_l2norm=True, gate="bounded",
+                    stream=None) -> Records:
+    """Plan + prep of the chunk-parallel prefill through ``kda_prefill_records``."""
+    T, H, dk = q.shape
+    dev = q.device
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    cu_host = cu_seqlens.to("cpu")
+    args = make_prefill_args(q, k, v, z, beta, A, cu_seqlens, cu_host, None, g_min=g_min,
+                             qk_l2norm=qk_l2norm, gate=gate)
+    need = prefill_workspace_size(args)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    ws[:4].zero_()
+    args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
+    _check(load_library().kda_prefill_records(ctypes.byref(args), _stream(stream)), "kda_prefill_records")
+    return Records(args, (q, k, v, z, beta, A, cu_seqlens, cu_host), ws, (T, H, dk, v.shape[2], cu_host.numel() - 1))
+
+
+def prefill_scan(rec: Records, S0=None, g_in=None, norm_w=None, scale=1.0, norm_eps=1e-6, want_o=True,
+                 want_state=True, zero_v=False, stream=None):
+    """The state recurrence over ``rec`` through ``kda_prefill_scan``: returns
+    (o, S_T, y) exactly as ``prefill`` would for the same inputs and S0
+    (with v taken as zero when ``zero_v``)."""
+    T, H, dk, dv, N = rec.shape
+    dev = rec.workspace.device
+    q = rec.keep[0]
+    args = PrefillArgs.from_buffer_copy(rec.args)
+    o = torch.empty((T, H, dv), dtype=q.dtype, device=dev) if want_o else None
+    S_T = torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev) if want_state else None
+    y = torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev) if g_in is not None else None
+    for name, t in (("o", o), ("S0", S0), ("S_T", S_T), ("g_in", g_in), ("norm_w", norm_w), ("y", y)):
+        setattr(args, name, t.data_ptr() if t is not None else None)
+    args.scale, args.norm_eps = float(scale), float(norm_eps)
+    _check(load_library().kda_prefill_scan(ctypes.byref(args), SCAN_ZERO_V if zero_v else 0, _stream(stream)),
+           "kda_prefill_scan")
     return o, S_T, y
 
 

@@ -171,3 +171,27 @@ def test_status_strings(kda_lib):
     assert b"cu_seqlens" in kda_lib.kda_status_str(5)
     kda_lib.kda_version.restype = ctypes.c_char_p
     assert b"sm_103a" in kda_lib.kda_version()
+
+
+def test_records_and_scan_validation(kda_lib):
+    """kda_prefill_records / kda_prefill_scan: kda_prefill's argument checks,
+    then the chunk-parallel workspace, the flags and the schedule's inputs."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    a, cu = _args(kda)
+    need = kda_lib.kda_prefill_workspace_size(ctypes.byref(a))
+    assert need > 256
+    for mutate, expect in ((dict(q=None), 1), (dict(T_total=65), 5), (dict(dk=96, dv=96), 2),
+                           (dict(o=FAKE + 8), 4)):
+        b, _c = _args(kda, **mutate)
+        assert kda_lib.kda_prefill_records(ctypes.byref(b), None) == expect
+        assert kda_lib.kda_prefill_scan(ctypes.byref(b), 0, None) == expect
+    assert kda_lib.kda_prefill_records(ctypes.byref(a), None) == 8          # no workspace
+    a.workspace, a.workspace_bytes = FAKE, need - 1
+    assert kda_lib.kda_prefill_scan(ctypes.byref(a), 0, None) == 8         # smaller than the records
+    a.workspace, a.workspace_bytes = FAKE + 8, need
+    assert kda_lib.kda_prefill_records(ctypes.byref(a), None) == 4         # misaligned
+    a.workspace = FAKE
+    assert kda_lib.kda_prefill_scan(ctypes.byref(a), 2, None) == 2         # unknown flag
+    f, _c2 = _args(kda, qkv_dtype=kda.KDA_F32, workspace=FAKE, workspace_bytes=1 << 40)
+    assert kda_lib.kda_prefill_records(ctypes.byref(f), None) == 6         # no chunk-parallel schedule
+    assert kda_lib.kda_prefill_scan(ctypes.byref(f), kda.SCAN_ZERO_V, None) == 6

@@ -100,3 +100,32 @@ def test_local_kcp_full_size_eight_segments(kda_lib, cuda_dev):
     ds = I.make_prefill(w, heads=heads)
     ro, rS, _ = oracle.prefill(f64(ds, "q"), f64(ds, "k"), f64(ds, "v"), ds["z"], ds["beta"], ds["A"])
     assert rel(host(o[:, heads]), ro) < TOL_O and rel(host(S_kcp[heads]), rS[0]) < TOL_S
+
+
+def test_records_then_scans_equal_prefill(kda_lib, cuda_dev):
+    """kda_prefill_records + kda_prefill_scan give kda_prefill's results bit for
+    bit (packed ragged sequences incl. an empty one, S0, the fused gate), several
+    scans over one set of records agree, and the zero-v scan equals a prefill
+    with v = 0 (the KCP transition M)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    cu = [0, 1, 130, 130, 449, 700]
+    H = 3
+    d = I.make_prefill(I.workload("prefill_128k", T=cu[-1], H=H))
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
+    cu_d = torch.tensor(cu, dtype=torch.int32, device=cuda_dev)
+    S0 = torch.randn((len(cu) - 1, H, 128, 128), generator=torch.Generator().manual_seed(5)).to(cuda_dev) / 8
+    g_in = torch.randn((cu[-1], H, 128), generator=torch.Generator().manual_seed(6)).to(cuda_dev).to(torch.bfloat16)
+    o1, S1, y1 = kda.prefill(q, k, v, z, beta, A, cu_seqlens=cu_d, S0=S0, g_in=g_in)
+    rec = kda.prefill_records(q, k, v, z, beta, A, cu_seqlens=cu_d)
+    for _ in range(2):
+        o2, S2, y2 = kda.prefill_scan(rec, S0=S0, g_in=g_in)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(S1, S2) and torch.equal(y1, y2)
+    _, Sz, _ = kda.prefill_scan(rec, want_o=False)                       # from zero, records reused
+    _, Sz1, _ = kda.prefill(q, k, v, z, beta, A, cu_seqlens=cu_d, want_o=False)
+    assert torch.equal(Sz, Sz1)
+    o3, S3, _ = kda.prefill_scan(rec, S0=S0, zero_v=True)
+    o4, S4, _ = kda.prefill(q, k, torch.zeros_like(v), z, beta, A, cu_seqlens=cu_d, S0=S0)
+    torch.cuda.synchronize()
+    assert torch.equal(o3, o4) and torch.equal(S3, S4)
