@@ -818,7 +818,9 @@ struct ScanCfg {
     static constexpr int G_TILE = C * NE * 2;                // g_in tile, [C][NE] bf16
     static constexpr int OFF_G0 = OFF_VOP + NE * C * 4;
     static constexpr int OFF_G1 = OFF_G0 + G_TILE;
-    static constexpr int OFF_SMALL = OFF_G1 + G_TILE;
+    static constexpr int KT_BYTES = 128 * C * 4;             // (K gamma_C / Gamma)^T, SW128 [128 rows][C]
+    static constexpr int OFF_RK = OFF_G1 + G_TILE;           // its staging buffer (one chunk)
+    static constexpr int OFF_SMALL = OFF_RK + KT_BYTES;
     // small region (floats): peers' row sums [2 parity][R source][C], own halves [2][2][C],
     // RMSNorm weights of this CTA's columns [NE]
     static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_NORMW = SM_ROWPART + 4 * C;
@@ -829,10 +831,17 @@ struct ScanCfg {
     static constexpr uint32_t TM_DS = TM_A3 + 2 * C;         // NE cols: state increment
     static constexpr uint32_t TM_S = TM_DS + NE;             // NE cols: FP32 state
     static constexpr uint32_t TM_COLS = (TM_S + NE) <= 256 ? 256 : 512;
-    static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0, "1024-B aligned operands");
+    static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0 && OFF_RK % 1024 == 0,
+                  "1024-B aligned operands");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(TM_S + NE <= TM_COLS, "TMEM budget");
 };
+
+// shared memory -> TMEM: 128 lanes x 256 bits (8 fp32 columns) from the
+// matrix the descriptor describes (the layout an MMA reads as one K = 8 step)
+TC_DEV void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
 
 // 4-byte store into a peer CTA's shared memory that completes 4 transaction bytes
 // on the peer's mbarrier (no fence: the mbarrier phase carries the data)
@@ -873,7 +882,7 @@ TC_DEV uint32_t gtile_offset(int row, int col) {
 template <int R>
 __global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(NT, 1)
 scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
-            const __grid_constant__ CUtensorMap tm_g) {
+            const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_kt) {
     using Cfg = ScanCfg<R>;
     constexpr int NE = Cfg::NE;
     constexpr int HW = NE / 2;           // value columns per thread
@@ -890,7 +899,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint64_t* bar_g = mbar + 3;          // [2]
     uint64_t* bar_full = mbar + 5;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
     uint64_t* bar_free = mbar + 7;       // [2][R] peer p has read this CTA's row sums of chunk j
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 7 + 2 * R);
+    uint64_t* bar_rk = mbar + 7 + 2 * R; // staged (K gamma_C / Gamma)^T landed
+    uint64_t* bar_ck = bar_rk + 1;       // its copy into TMEM is done (the staging buffer is free)
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_rk + 2);
 
     const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
@@ -919,8 +930,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             tc::mbar_init(bar_full + b, 1);
             for (int p = 0; p < R; ++p) tc::mbar_init(bar_free + b * R + p, 1);
         }
+        tc::mbar_init(bar_rk, 1);
+        tc::mbar_init(bar_ck, 1);
         tc::mbar_fence_init();
         tc::tma_prefetch_desc(&tm_aw);
+        tc::tma_prefetch_desc(&tm_kt);
         if (gate) tc::tma_prefetch_desc(&tm_g);
         for (int j = 0; j < 2 && j < nch; ++j) {
             tc::mbar_arrive_expect_tx(bar_aw + j, Cfg::AW_TILE);
@@ -954,17 +968,16 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     };
 
     // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
-    // CTA's columns; (K gamma_C / Gamma)^T row `row`, tokens 32*hf..32*hf+31; gamma_C[row]
-    float pu[HW], pk[32], pg = 0.f;
+    // CTA's columns, and gamma_C[row]; (K gamma_C / Gamma)^T, the same for the
+    // four CTAs, goes by TMA into a staging buffer and from there by tcgen05.cp
+    // into TMEM, both issued by thread 0
+    float pu[HW], pg = 0.f;
     auto load_rec = [&](int j) {
         const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
-        const float* k = w.kt + rec_of(j) * KT_FLOATS + (size_t)row * C + 32 * hf;
         if (!w.zero_v) {
 #pragma unroll
             for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ld_nc_f8(k + 8 * i, pk + 8 * i);
         pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
     };
     auto store_rec = [&](int b) {
@@ -973,9 +986,23 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             for (int i = 0; i < HW; i += 16)
                 tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
         }
+    };
+    uint8_t* sRk = sm + Cfg::OFF_RK;
+    uint32_t ph_rk = 0, ph_ck = 0;   // thread 0's phases
+    auto tma_k = [&](int j) {
+        tc::mbar_arrive_expect_tx(bar_rk, Cfg::KT_BYTES);
 #pragma unroll
-        for (int i = 0; i < 32; i += 16)
-            tc::tmem_st16(T0 + Cfg::TM_A3 + C * b + lane_base + 32 * hf + i, pk + i);
+        for (int s = 0; s < C / 32; ++s)
+            tc::tma_load_2d(sRk + s * (128 * 32 * 4), &tm_kt, 32 * s, (int)(rec_of(j) * 128), bar_rk);
+    };
+    auto cp_k = [&](int b) {   // staged (K gamma_C / Gamma)^T -> TMEM buffer b
+        wait(bar_rk, ph_rk);
+        ph_rk ^= 1u;
+        tc::fence_after_sync();
+        const uint32_t sk = tc::smem_u32(sRk);
+#pragma unroll
+        for (int kc = 0; kc < C / 8; ++kc)
+            tmem_cp_128x256b(T0 + Cfg::TM_A3 + C * b + 8 * kc, tc::sw128_desc_k(sk, 128, kc));
     };
     // o and y of chunk jo from its TMEM buffer (output-row threads, row >= C)
     auto emit_outputs = [&](int jo) {
@@ -1025,6 +1052,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     };
 
     // ---- initial state -> TMEM master copy and the tf32 operand copy
+    if (tid == 0 && nch > 0) tma_k(0);
     float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
     {
         const int d = row;
@@ -1044,6 +1072,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         tc::tmem_st_wait();
         tc::fence_proxy_async();
     }
+    if (tid == 0 && nch > 0) {
+        cp_k(0);
+        tc::mma_commit(mbar);
+    }
+    if (nch > 0) mma_wait();   // every thread: keeps the MMA phase in step
+    if (tid == 0 && nch > 1) tma_k(1);
     tc::fence_before_sync();
     __syncthreads();
     if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
@@ -1070,6 +1104,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             // the peers' row sums of this chunk (phase j - 2 of this barrier completed
             // before the previous chunk's closing __syncthreads)
             if (gate) tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4);
+            // the next chunk's (K gamma_C / Gamma)^T into TMEM buffer b ^ 1 (its last
+            // reader, MMA 3 of chunk j - 1, has completed)
+            if (j + 1 < nch) {
+                cp_k(b ^ 1);
+                tc::mma_commit(bar_ck);
+            }
         }
         // while it runs: outputs of the previous chunk (their buffer is refilled next),
         // the next record into the other TMEM buffers, the one after it into registers
@@ -1078,10 +1118,17 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         if (j + 2 < nch) load_rec(j + 2);
         tc::tmem_st_wait();
         mma_wait();
-        if (tid == 0 && j + 2 < nch) {   // the A tile of this chunk is consumed
-            tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
-            for (int s = 0; s < 4; ++s)
-                tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
+        if (tid == 0) {
+            if (j + 2 < nch) {   // the A tile of this chunk is consumed
+                tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
+                for (int s = 0; s < 4; ++s)
+                    tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
+            }
+            if (j + 1 < nch) {   // the staging buffer is free once its copy is done
+                wait(bar_ck, ph_ck);
+                ph_ck ^= 1u;
+                if (j + 2 < nch) tma_k(j + 2);
+            }
         }
 
         // ---- V' -> operand (smem); output rows: sums of squares for the gate
@@ -1300,6 +1347,9 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
                       NE == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
     if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.aw, 128, (uint64_t)L.nrec * 128, 32, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    CUtensorMap mkt;
+    if ((e = make_map(&mkt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.kt, spl::C, (uint64_t)L.nrec * 128, 32, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
 
     int launched = 0;
     if (parts & 1) {
@@ -1317,7 +1367,7 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     }
     if (parts & 2) {
         dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
-        spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg);
+        spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
         ++launched;
     }
     count_launches(launched);
