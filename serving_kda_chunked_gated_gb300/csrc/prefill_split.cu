@@ -639,7 +639,6 @@ prep_kernel(kda_prefill_args a, Work w,
             const int i = row & 63;
             const float* src = (row < C ? sT : sAqk) + i * AS;
             float v[16];
-#pragma unroll
             {
                 const int c = 16 * grp;
 #pragma unroll
