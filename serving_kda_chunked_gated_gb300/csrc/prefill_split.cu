@@ -83,6 +83,14 @@ TC_DEV uint32_t sw128_bf16(int row, int col) {
 TC_DEV float4 ld_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 // After a wait gave up anywhere in the CTA, give copies still in flight into
 // this CTA's shared memory about a millisecond to land before it is released.
+// four 8 x 4 fp32 matrices from shared memory (ldmatrix on 16-bit pairs): lane l
+// passes the address of row l & 7 of matrix l >> 3 (16-byte aligned) and gets
+// word (l & 3) of row (l >> 2) of each matrix -- the tf32 m16n8k8 fragment order
+TC_DEV void ldsm_x4(const float* p, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(tc::smem_u32(p)) : "memory");
+}
+
 TC_DEV void drain_if(bool timed_out) {
     if (__syncthreads_or(timed_out) && threadIdx.x == 0)
         for (int i = 0; i < 1000; ++i) __nanosleep(1000);
@@ -467,15 +475,20 @@ prep_kernel(kda_prefill_args a, Work w,
                 for (int it = 0; it < 2; ++it) {
                     if ((it == 0 || (ks >> 2) == kq) && !(GATE && ia[it] == ib[it])) {
                         const float* Arows = kk[it] ? sKr : sQ;
-                        const int ra = 16 * ia[it] + g;
-                        const float af[4] = {tc::to_tf32(Arows[ra * QS + k0]), tc::to_tf32(Arows[(ra + 8) * QS + k0]),
-                                             tc::to_tf32(Arows[ra * QS + k1]), tc::to_tf32(Arows[(ra + 8) * QS + k1])};
+                        const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: this lane's matrix and row
+                        uint32_t ra4[4], rb4[4];
+                        // A: rows 16 ia + (0..7 | 8..15), columns 8 ks + (0..3 | 4..7)
+                        ldsm_x4(Arows + (16 * ia[it] + mr + 8 * (mi & 1)) * QS + 8 * ks + 4 * (mi >> 1), ra4);
+                        // B: rows 16 ib + 8 nh + (0..7), columns 8 ks + (0..3 | 4..7), nh = mi >> 1
+                        ldsm_x4(sK + (16 * ib[it] + 8 * (mi >> 1) + mr) * QS + 8 * ks + 4 * (mi & 1), rb4);
+                        const float af[4] = {tc::to_tf32(__uint_as_float(ra4[0])), tc::to_tf32(__uint_as_float(ra4[1])),
+                                             tc::to_tf32(__uint_as_float(ra4[2])), tc::to_tf32(__uint_as_float(ra4[3]))};
                         const float* ct = s_ctab + (ia[it] * (ia[it] + 1) / 2 + ib[it]) * D;
                         const float c0f = ct[k0], c1f = ct[k1];
 #pragma unroll
                         for (int nh = 0; nh < 2; ++nh) {
-                            const int j = 16 * ib[it] + 8 * nh + g;
-                            const float bfr[2] = {tc::to_tf32(sK[j * QS + k0] * c0f), tc::to_tf32(sK[j * QS + k1] * c1f)};
+                            const float bfr[2] = {tc::to_tf32(__uint_as_float(rb4[2 * nh]) * c0f),
+                                                  tc::to_tf32(__uint_as_float(rb4[2 * nh + 1]) * c1f)};
                             tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
                         }
                     }
