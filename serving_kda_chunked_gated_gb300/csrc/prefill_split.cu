@@ -561,12 +561,15 @@ prep_kernel(kda_prefill_args a, Work w,
             const int g = lane >> 2, t4 = lane & 3;
             float* wsc = sW + warp * 16 * 16;
             auto blk = [&](float* M, int a_, int b_) { return M + (16 * a_) * AS + 16 * b_; };
+            const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: this lane's matrix and row
             auto mma16 = [&](float (&acc)[2][4], const float* X, const float* Y, int ly) {
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     const int k0 = 8 * ks + t4, k1 = k0 + 4;
-                    const float af[4] = {tc::to_tf32(X[g * AS + k0]), tc::to_tf32(X[(g + 8) * AS + k0]),
-                                         tc::to_tf32(X[g * AS + k1]), tc::to_tf32(X[(g + 8) * AS + k1])};
+                    uint32_t ra4[4];   // X rows (0..7 | 8..15), columns 8 ks + (0..3 | 4..7); X has row stride AS
+                    ldsm_x4(X + (mr + 8 * (mi & 1)) * AS + 8 * ks + 4 * (mi >> 1), ra4);
+                    const float af[4] = {tc::to_tf32(__uint_as_float(ra4[0])), tc::to_tf32(__uint_as_float(ra4[1])),
+                                         tc::to_tf32(__uint_as_float(ra4[2])), tc::to_tf32(__uint_as_float(ra4[3]))};
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
                         const int nn = 8 * nh + g;
