@@ -1139,11 +1139,6 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int s = 0; s < 4; ++s)
                     tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
             }
-            if (j + 1 < nch) {   // the staging buffer is free once its copy is done
-                wait(bar_ck, ph_ck);
-                ph_ck ^= 1u;
-                if (j + 2 < nch) tma_k(j + 2);
-            }
         }
 
         // ---- V' -> operand (smem); output rows: sums of squares for the gate
@@ -1185,6 +1180,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::mma_tf32_ts(T0 + Cfg::TM_DS, T0 + Cfg::TM_A3 + C * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
                                 tc::idesc_tf32(128, NE), ks > 0);
             tc::mma_commit(mbar);
+            if (j + 1 < nch) {   // the staging buffer is free once the K copy is done (waited
+                                 // here, after the chunk's first barrier, off the path into it)
+                wait(bar_ck, ph_ck);
+                ph_ck ^= 1u;
+                if (j + 2 < nch) tma_k(j + 2);
+            }
             // the g_in tile of chunk j-1 is consumed (its outputs were emitted above)
             if (gate && j >= 1 && j + 1 < nch) {
                 tc::mbar_arrive_expect_tx(bar_g + (b ^ 1), Cfg::G_TILE);
