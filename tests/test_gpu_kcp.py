@@ -129,3 +129,24 @@ def test_records_then_scans_equal_prefill(kda_lib, cuda_dev):
     o4, S4, _ = kda.prefill(q, k, torch.zeros_like(v), z, beta, A, cu_seqlens=cu_d, S0=S0)
     torch.cuda.synchronize()
     assert torch.equal(o3, o4) and torch.equal(S3, S4)
+
+
+def test_local_kcp_without_records_fp32(kda_lib, cuda_dev):
+    """fp32 inputs with d = 64 have no chunk-parallel schedule: GpuOps then takes
+    three kda_prefill calls per segment (per-token recurrence); the KCP result
+    still equals the single pass and the oracle."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    from serving_kda_chunked_gated_gb300 import kcp
+    T, cuts = 300, [0, 100, 101, 300]
+    d = I.make_prefill(I.workload("tiny", T=T, H=2, dk=64, dv=64))
+    segs = _segments(d, cuda_dev, cuts)
+    ops = kcp.GpuOps()
+    assert ops._records(segs[0]) is None
+    outs = kcp.kcp_prefill_local(segs, ops)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    o1, S1, _ = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev))
+    torch.cuda.synchronize()
+    o = torch.cat([x[0] for x in outs])
+    assert rel(host(o), host(o1)) < TOL_O and rel(host(outs[-1][1]), host(S1[0])) < TOL_S
+    ro, rS, _ = oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"])
+    assert rel(host(o), ro) < TOL_O and rel(host(outs[-1][1]), rS[0]) < TOL_S
