@@ -121,3 +121,52 @@ def test_kcp_local_driver_and_pair_composition():
     M12, S12 = ops.pair(seg12)
     np.testing.assert_allclose(torch.matmul(M2, M1).numpy(), M12.numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(ops.apply(M2, S1, S2).numpy(), S12.numpy(), rtol=0, atol=1e-12)
+
+
+def _fake_seg(dtype, T=3, H=2, d=128):
+    seg = {key: torch.zeros((T, H, d), dtype=dtype) for key in ("q", "k")}
+    seg["v"] = torch.ones((T, H, d), dtype=dtype)
+    seg.update(z=torch.zeros((T, H, d)), beta=torch.zeros((T, H)), A=torch.zeros(H))
+    return seg
+
+
+def test_gpu_ops_share_one_set_of_records_per_segment(monkeypatch):
+    """GpuOps builds a segment's chunk records once: the pair is two scans over
+    them (M with the zero-v flag from S0 = I, S~ from zero), the segment's
+    outputs a third; the records are released after it.  Inputs without a
+    chunk-parallel schedule (fp32) take three kda_prefill calls instead."""
+    sys.path.insert(0, ROOT)
+    from serving_kda_chunked_gated_gb300 import kcp, kda
+    calls = []
+
+    def fake_records(q, k, v, z, beta, A, **kw):
+        calls.append(("records",))
+        return object()
+
+    def fake_scan(rec, S0=None, g_in=None, norm_w=None, want_o=True, want_state=True, zero_v=False, **kw):
+        H, d = 2, 128
+        eye = S0 is not None and torch.equal(S0[0, 0], torch.eye(d))
+        calls.append(("scan", zero_v, eye, S0 is None, want_o))
+        return (torch.zeros((3, H, d)) if want_o else None), torch.zeros((1, H, d, d)), None
+
+    def fake_prefill(q, k, v, z, beta, A, S0=None, want_o=True, **kw):
+        calls.append(("prefill", bool((v == 0).all()), S0 is not None, want_o))
+        H, d = q.shape[1], q.shape[2]
+        return (torch.zeros((3, H, d)) if want_o else None), torch.zeros((1, H, d, d)), None
+
+    monkeypatch.setattr(kda, "prefill_records", fake_records)
+    monkeypatch.setattr(kda, "prefill_scan", fake_scan)
+    monkeypatch.setattr(kda, "prefill", fake_prefill)
+    ops = kcp.GpuOps()
+    seg = _fake_seg(torch.bfloat16)
+    M, St = ops.pair(seg)
+    assert M.shape == (2, 128, 128) and St.shape == (2, 128, 128)
+    ops.prefill(seg, torch.zeros((2, 128, 128)))
+    assert calls == [("records",), ("scan", True, True, False, False), ("scan", False, False, True, False),
+                     ("scan", False, False, False, True)]
+    assert ops._rec == {}
+    calls.clear()
+    seg32 = _fake_seg(torch.float32, d=64)
+    ops.pair(seg32)
+    ops.prefill(seg32, torch.zeros((2, 64, 64)))
+    assert calls == [("prefill", True, True, False), ("prefill", False, False, False), ("prefill", False, True, True)]
