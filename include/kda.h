@@ -46,7 +46,9 @@ typedef enum {
     KDA_ERR_SEQLENS = 5,     /* cu_seqlens not monotone / not ending at tokens    */
     KDA_ERR_UNSUPPORTED = 6, /* valid request the library does not implement      */
     KDA_ERR_CUDA = 7,        /* a CUDA runtime call or a launch failed            */
-    KDA_ERR_WORKSPACE = 8    /* workspace missing or smaller than required        */
+    KDA_ERR_WORKSPACE = 8,   /* workspace missing or smaller than required        */
+    KDA_ERR_TIMEOUT = 9      /* a bounded wait inside a kernel gave up (read by
+                                kda_get_last_device_error; see there)            */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -104,9 +106,12 @@ typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
  *    (one cluster per (sequence, head) walks its chunks); no scratch beyond
  *    the error word.
  *  - less: KDA_ERR_WORKSPACE.
- * The first 4 bytes of the workspace are an error word: a wait inside a
- * kernel that gave up ORs 1 into it (zero it before the call to read it).
- * The CUDA-core path needs no workspace (size 0; may be NULL).
+ * The first 4 bytes of the workspace are the call's error word: kda_prefill
+ * and kda_prefill_records clear it on the stream before their kernels run,
+ * kda_prefill_scan does not (a records call's word stays visible through its
+ * scans), and a bounded wait inside a kernel that gives up sets it; read it
+ * with kda_get_last_device_error.  The CUDA-core path needs no workspace
+ * (size 0; may be NULL) and has no waits.
  */
 #define KDA_PREFILL_MIN_WORKSPACE 256
 typedef struct {
@@ -206,8 +211,16 @@ kda_status kda_prefill_scan(const kda_prefill_args* args, int flags, void* strea
  *    each call clears what must start at zero (with cudaMemsetAsync on the
  *    caller's stream).  Calls that overlap on the GPU (different streams with
  *    no ordering between them) race on the array: serialise them.
- *  - The first call on each device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - Each call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress: no allocation, nothing cached across calls, so a
+ *    device reset that reloads the library's module leaves no stale address).
+ *    The first call on a device loads the module there; make that first call
+ *    before any stream capture.
+ *  - A bounded wait that gives up is recorded in the array's error word; read
+ *    it with kda_get_last_device_error(NULL, stream).  The size check above
+ *    cannot reject a call at the current sizes (the single-pass schedule
+ *    needs KDA_PREFILL_MIN_WORKSPACE bytes, the CUDA-core path none); it
+ *    guards future schedules.
  * Inputs and outputs are the caller's, exactly as for kda_prefill.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES 4096
@@ -348,6 +361,39 @@ kda_status kda_short_conv_step(const kda_short_conv_step_args* args, void* strea
  *   overlap M or add; 1 <= d <= 256, n >= 1; all device memory, 16-byte aligned.
  */
 kda_status kda_kcp_apply(const float* M, float* X, const float* add, int H, int d, int n, void* stream);
+
+/*
+ * Device-side error report of the tensor-core prefill (library plumbing: the
+ * KDA pages have no counterpart).  Every wait of a prefill kernel on an
+ * asynchronous copy, a tensor-core operation or a peer CTA is bounded; a wait
+ * that runs out records it in the call's error word, stops issuing new
+ * asynchronous work, waits (again bounded) for the copies and tensor-core
+ * operations it has already issued, and lets the kernel finish, so the CUDA
+ * context stays usable.  The call's outputs are then invalid.
+ *
+ * kda_get_last_device_error waits for the work queued on `stream`, then reads
+ * and clears the error word of `workspace` (the workspace the prefill calls
+ * used), or, with workspace == NULL, of the fixed array kda_prefill_noalloc
+ * uses on the current device.  Returns KDA_OK when no wait gave up,
+ * KDA_ERR_TIMEOUT when one did, KDA_ERR_CUDA when the read failed.  It
+ * allocates nothing.  Call it on the stream of the prefill calls (or after
+ * synchronising them); calls on other streams that use the same workspace
+ * must not run concurrently.
+ */
+kda_status kda_get_last_device_error(void* workspace, void* stream);
+
+/*
+ * Test hook: the number of polls after which a bounded wait of the prefill
+ * kernels on a copy or a tensor-core operation gives up, for every launch
+ * that follows (from any thread).  KDA_WAIT_LIMIT_DEFAULT restores the
+ * default (about 4 million polls: seconds); 0 makes every such wait give up
+ * at once, which exercises, deterministically, the path that
+ * kda_get_last_device_error reports.  Waits between the CTAs of a cluster and
+ * the final waits before a CTA exits keep their default bound.  Returns the
+ * previous setting.
+ */
+#define KDA_WAIT_LIMIT_DEFAULT 0xFFFFFFFFu
+uint32_t kda_debug_set_wait_limit(uint32_t polls);
 
 /* Static description of a status code. */
 const char* kda_status_str(kda_status s);

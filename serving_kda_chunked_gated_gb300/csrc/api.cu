@@ -4,7 +4,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kda_common.cuh"
+#include "tcgen05.cuh"
 
 namespace kda {
 cudaError_t launch_decode_step(const kda_decode_args& a, cudaStream_t stream);
@@ -22,14 +25,21 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
 cudaError_t launch_short_conv(const kda_short_conv_args& a, cudaStream_t s);
 cudaError_t launch_kcp_apply(const float* M, float* X, const float* Add, int H, int d, int n, cudaStream_t s);
 cudaError_t launch_short_conv_step(const kda_short_conv_step_args& a, cudaStream_t s);
+cudaError_t noalloc_scratch_address(void** out);
 }  // namespace kda
 
 static thread_local char g_last_error[256] = "no error";
 static thread_local uint64_t g_launches = 0;
+static std::atomic<uint32_t> g_wait_limit{KDA_WAIT_LIMIT_DEFAULT};   // kda_debug_set_wait_limit
 
 namespace kda {
 // called by every launch wrapper once per kernel enqueued
 void count_launches(int n) { g_launches += (uint64_t)n; }
+// poll bound of the prefill kernels' waits on local copies and MMAs
+uint32_t wait_limit() {
+    const uint32_t v = g_wait_limit.load(std::memory_order_relaxed);
+    return v == KDA_WAIT_LIMIT_DEFAULT ? tc::WAIT_POLLS : v;
+}
 }  // namespace kda
 
 static kda_status cuda_fail(cudaError_t e) {
@@ -52,11 +62,27 @@ const char* kda_status_str(kda_status s) {
         case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
         case KDA_ERR_CUDA: return "CUDA error";
         case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up (outputs invalid)";
     }
     return "unknown status";
 }
 
 const char* kda_last_error_string(void) { return g_last_error; }
+
+kda_status kda_get_last_device_error(void* workspace, void* stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void* word = workspace;
+    cudaError_t e = cudaSuccess;
+    if (!word && (e = kda::noalloc_scratch_address(&word)) != cudaSuccess) return cuda_fail(e);
+    if (misaligned(word)) return KDA_ERR_ALIGN;
+    int32_t h = 0;
+    if ((e = cudaMemcpyAsync(&h, word, sizeof(h), cudaMemcpyDeviceToHost, s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemsetAsync(word, 0, sizeof(h), s)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e);
+    return h ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
+uint32_t kda_debug_set_wait_limit(uint32_t polls) { return g_wait_limit.exchange(polls); }
 
 uint64_t kda_launch_count(void) { return g_launches; }
 

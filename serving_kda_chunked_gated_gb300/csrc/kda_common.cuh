@@ -12,6 +12,9 @@ namespace kda {
 
 // launch accounting (api.cu): every launch wrapper reports the kernels it enqueued
 void count_launches(int n);
+// poll bound of the prefill kernels' waits on local copies and MMAs (api.cu;
+// kda_debug_set_wait_limit)
+uint32_t wait_limit();
 
 // Logistic function through the hardware exp2 / fast-divide path.
 KDA_DEV float sigmoidf_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }

@@ -60,9 +60,10 @@ struct Work {
     float* uu;
     float* kt;
     float* gm;
-    int* err;                // bounded waits that gave up set bit 0
+    int* err;                // error word: tc::ERR_WAIT | tc::ERR_DRAIN
     long nrec;               // chunks * H
     int zero_v;              // scan: take v as zero (the U records are not read)
+    uint32_t wait_limit;     // polls before a wait on a local copy or MMA gives up
 };
 
 TC_DEV uint32_t cluster_map(const void* p, uint32_t rank) {
@@ -81,8 +82,6 @@ TC_DEV uint32_t sw128_bf16(int row, int col) {
     return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 TC_DEV float4 ld_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
-// After a wait gave up anywhere in the CTA, give copies still in flight into
-// this CTA's shared memory about a millisecond to land before it is released.
 // four 8 x 4 fp32 matrices from shared memory (ldmatrix on 16-bit pairs): lane l
 // passes the address of row l & 7 of matrix l >> 3 (16-byte aligned) and gets
 // word (l & 3) of row (l >> 2) of each matrix -- the tf32 m16n8k8 fragment order
@@ -91,19 +90,18 @@ TC_DEV void ldsm_x4(const float* p, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(tc::smem_u32(p)) : "memory");
 }
 
-TC_DEV void drain_if(bool timed_out) {
-    if (__syncthreads_or(timed_out) && threadIdx.x == 0)
-        for (int i = 0; i < 1000; ++i) __nanosleep(1000);
-}
-
 // ---------------------------------------------------------------------------
-// plan: chunk_base[n] = sum_{m < n} ceil(len_m / C), n = 0..num_seqs (one CTA)
+// plan: chunk_base[n] = sum_{m < n} ceil(len_m / C), n = 0..num_seqs (one CTA);
+// also clears the call's error word
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs, int* chunk_base) {
+__global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs, int* chunk_base, int* err) {
     __shared__ int s_warp[32];
     __shared__ int s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_carry = 0;
+    if (tid == 0) {
+        s_carry = 0;
+        *err = 0;   // the call's error word starts clear (the kernels after this one set it)
+    }
     __syncthreads();
     for (int base = 0; base < num_seqs; base += 1024) {
         const int n = base + tid;
@@ -281,6 +279,9 @@ prep_kernel(kda_prefill_args a, Work w,
         const int t0 = s_loc[14] + C * (int)(g - s_loc[12]);
         s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hn;
     }
+    // thread 0 issues every copy and MMA; it counts the phases it issued on each
+    // mbarrier, for the give-up path at the end
+    uint32_t n_in = 0, n_v = 0, n_mma = 0;
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
         tc::mbar_init(bar_in, 1);
@@ -298,6 +299,7 @@ prep_kernel(kda_prefill_args a, Work w,
             tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
             tc::tma_load_2d(sm + OFF_RAWV, &tm_v, cur.h * D, cur.t0, bar_v);
             tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, cur.h * D + 64, cur.t0, bar_v);
+            n_in = n_v = 1;
         }
     }
     tc::fence_before_sync();
@@ -306,10 +308,11 @@ prep_kernel(kda_prefill_args a, Work w,
     const uint32_t T0 = *tbase_ptr;
     uint32_t ph_mma = 0, ph_in = 0, ph_v = 0;
     bool timed_out = false;
-    // a wait that gives up records it, and every later wait is skipped so that
-    // the kernel runs to its end quickly (its results are then invalid)
+    // A wait that gives up records it; this thread then skips every later wait,
+    // and thread 0 issues no further copy or MMA, so the kernel runs to its end
+    // quickly (its results are then invalid) and drains what was issued.
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
+        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, w.wait_limit)) timed_out = true;
     };
     float beta_next = 0.f;
     if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
@@ -714,7 +717,8 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
         // the raw v tiles are consumed: fetch the next record's
-        if (tid == 0 && has_next) {
+        if (tid == 0 && has_next && !timed_out) {
+            ++n_v;
             tc::fence_proxy_async();
             tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
             tc::tma_load_2d(sm + OFF_RAWV, &tm_v, nxt.h * D, nxt.t0, bar_v);
@@ -722,7 +726,8 @@ prep_kernel(kda_prefill_args a, Work w,
         }
 
         // ---- 5. MMA 1: D[:, 0:256] = [T beta ; P beta] . [V | Gamma K]
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
+            ++n_mma;
             tc::fence_after_sync();
             const uint32_t bb = tc::smem_u32(sBpre);
 #pragma unroll
@@ -735,7 +740,8 @@ prep_kernel(kda_prefill_args a, Work w,
         ph_mma ^= 1u;
         tc::fence_after_sync();
         // region RB is free again: fetch the next record's q, k, z into it
-        if (tid == 0 && has_next) {
+        if (tid == 0 && has_next && !timed_out) {
+            ++n_in;
             tc::fence_proxy_async();
             tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
             tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, nxt.h * D, nxt.t0, bar_in);
@@ -810,8 +816,13 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
     }
-    if (timed_out && w.err) atomicOr(w.err, 1);
-    drain_if(timed_out);
+    // give-up path: wait for the copies and the MMA thread 0 issued before any
+    // of this CTA's shared memory or TMEM is released
+    if (__syncthreads_or(timed_out) && tid == 0) {
+        const bool drained = tc::drain_phase(bar_in, n_in) & tc::drain_phase(bar_v, n_v) &
+                             tc::drain_phase(mbar, n_mma);
+        atomicOr(w.err, drained ? tc::ERR_WAIT : tc::ERR_WAIT | tc::ERR_DRAIN);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(T0, TM_COLS);
@@ -937,6 +948,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
     if (tid < NE) s_normw[tid] = a.norm_w ? a.norm_w[NE * r + tid] : 1.f;
+    // thread 0 issues every copy and MMA and arms the row-sum barriers; it counts
+    // the phases it issued on each mbarrier, for the give-up path at the end
+    uint32_t n_aw[2] = {0, 0}, n_g[2] = {0, 0}, n_full[2] = {0, 0}, n_rk = 0, n_ck = 0, n_mma = 0;
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
         for (int b = 0; b < 2; ++b) {
@@ -952,6 +966,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         tc::tma_prefetch_desc(&tm_kt);
         if (gate) tc::tma_prefetch_desc(&tm_g);
         for (int j = 0; j < 2 && j < nch; ++j) {
+            ++n_aw[j];
+            if (gate) ++n_g[j];
             tc::mbar_arrive_expect_tx(bar_aw + j, Cfg::AW_TILE);
             for (int s = 0; s < 4; ++s)
                 tc::tma_load_2d(aw_buf(j) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + j);
@@ -966,15 +982,21 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     tc::fence_after_sync();
     const uint32_t T0 = *tbase_ptr;
     uint32_t ph_mma = 0;
-    bool timed_out = false;
-    // a wait that gives up records it, and every later wait is skipped (the loop
-    // keeps its cluster barriers, so the peer CTAs are never left waiting)
+    // A wait on a local copy or MMA that gives up records it in timed_out: this
+    // thread then skips every later such wait, and thread 0 issues no further
+    // copy or MMA, so the kernel runs to its end (its results are invalid) and
+    // drains what was issued.  The row-sum exchange with the peer CTAs keeps
+    // running (its data are then meaningless, its protocol intact) so that no
+    // peer is left waiting and no row sum lands after a CTA has exited; a wait
+    // of that exchange that gives up (a peer that stopped) sets xdead, after
+    // which this thread stops exchanging.
+    bool timed_out = false, xdead = false;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
-        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, 1u << 22)) timed_out = true;
+        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, w.wait_limit)) timed_out = true;
     };
     auto wait_cl = [&](uint64_t* bar, uint32_t parity) {
-        for (uint32_t i = 0; !timed_out && !mbar_try_wait_cluster(bar, parity); )
-            if (++i == (1u << 22)) timed_out = true;
+        for (uint32_t i = 0; !xdead && !mbar_try_wait_cluster(bar, parity); )
+            if (++i == tc::WAIT_POLLS) xdead = true;
     };
     auto mma_wait = [&]() {
         wait(mbar, ph_mma);
@@ -1005,6 +1027,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint8_t* sRk = sm + Cfg::OFF_RK;
     uint32_t ph_rk = 0, ph_ck = 0;   // thread 0's phases
     auto tma_k = [&](int j) {
+        ++n_rk;
         tc::mbar_arrive_expect_tx(bar_rk, Cfg::KT_BYTES);
 #pragma unroll
         for (int s = 0; s < C / 32; ++s)
@@ -1013,6 +1036,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     auto cp_k = [&](int b) {   // staged (K gamma_C / Gamma)^T -> TMEM buffer b
         wait(bar_rk, ph_rk);
         ph_rk ^= 1u;
+        if (timed_out) return;
         tc::fence_after_sync();
         const uint32_t sk = tc::smem_u32(sRk);
 #pragma unroll
@@ -1067,7 +1091,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     };
 
     // ---- initial state -> TMEM master copy and the tf32 operand copy
-    if (tid == 0 && nch > 0) tma_k(0);
+    if (tid == 0 && nch > 0) tma_k(0);   // before any wait: thread 0 has not timed out
     float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
     {
         const int d = row;
@@ -1089,10 +1113,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     }
     if (tid == 0 && nch > 0) {
         cp_k(0);
-        tc::mma_commit(mbar);
+        if (!timed_out) { ++n_mma; tc::mma_commit(mbar); }
     }
     if (nch > 0) mma_wait();   // every thread: keeps the MMA phase in step
-    if (tid == 0 && nch > 1) tma_k(1);
+    if (tid == 0 && nch > 1 && !timed_out) tma_k(1);
     tc::fence_before_sync();
     __syncthreads();
     if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
@@ -1108,22 +1132,30 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         //      the first step then ignores the accumulator)
         if (tid == 0) {
             wait(bar_aw + b, (j >> 1) & 1);
-            tc::fence_after_sync();
-            const uint32_t ab = tc::smem_u32(aw_buf(b));
-            const uint32_t sb = tc::smem_u32(sSop);
+            if (!timed_out) {
+                tc::fence_after_sync();
+                const uint32_t ab = tc::smem_u32(aw_buf(b));
+                const uint32_t sb = tc::smem_u32(sSop);
 #pragma unroll
-            for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks), tc::sw128_desc_k(sb, NE, ks),
-                                tc::idesc_tf32(128, NE), (ks > 0 || !w.zero_v) ? 1u : 0u);
-            tc::mma_commit(mbar);
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks),
+                                    tc::sw128_desc_k(sb, NE, ks), tc::idesc_tf32(128, NE),
+                                    (ks > 0 || !w.zero_v) ? 1u : 0u);
+                ++n_mma;
+                tc::mma_commit(mbar);
+            }
             // the peers' row sums of this chunk (phase j - 2 of this barrier completed
-            // before the previous chunk's closing __syncthreads)
-            if (gate) tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4);
+            // before the previous chunk's closing __syncthreads; a peer that stopped
+            // leaves it open, and then the barrier is not armed again)
+            if (gate && !xdead) {
+                if (j >= 2 && !tc::mbar_try_wait(bar_full + b, ((j - 2) >> 1) & 1)) xdead = true;
+                else { ++n_full[b]; tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4); }
+            }
             // the next chunk's (K gamma_C / Gamma)^T into TMEM buffer b ^ 1 (its last
             // reader, MMA 3 of chunk j - 1, has completed)
-            if (j + 1 < nch) {
+            if (j + 1 < nch && !timed_out) {
                 cp_k(b ^ 1);
-                tc::mma_commit(bar_ck);
+                if (!timed_out) { ++n_ck; tc::mma_commit(bar_ck); }
             }
         }
         // while it runs: outputs of the previous chunk (their buffer is refilled next),
@@ -1133,8 +1165,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         if (j + 2 < nch) load_rec(j + 2);
         tc::tmem_st_wait();
         mma_wait();
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
             if (j + 2 < nch) {   // the A tile of this chunk is consumed
+                ++n_aw[b];
                 tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
                 for (int s = 0; s < 4; ++s)
                     tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
@@ -1172,22 +1205,29 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         __syncthreads();
 
         // ---- MMA 3: dS = (K gamma_C / Gamma)^T . V'
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
             tc::fence_after_sync();
             const uint32_t vb = tc::smem_u32(sVop);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks)
                 tc::mma_tf32_ts(T0 + Cfg::TM_DS, T0 + Cfg::TM_A3 + C * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
                                 tc::idesc_tf32(128, NE), ks > 0);
+            ++n_mma;
             tc::mma_commit(mbar);
             if (j + 1 < nch) {   // the staging buffer is free once the K copy is done (waited
                                  // here, after the chunk's first barrier, off the path into it)
                 wait(bar_ck, ph_ck);
                 ph_ck ^= 1u;
-                if (j + 2 < nch) tma_k(j + 2);
+                if (j + 2 < nch && !timed_out) tma_k(j + 2);
             }
-            // the g_in tile of chunk j-1 is consumed (its outputs were emitted above)
-            if (gate && j >= 1 && j + 1 < nch) {
+            // the g_in tile of chunk j-1 is consumed (its outputs were emitted above;
+            // the output-row threads waited for it, so its phase is complete unless
+            // one of their waits gave up -- then nothing more is issued)
+            if (gate && j >= 1 && j + 1 < nch && !timed_out &&
+                !tc::mbar_try_wait(bar_g + (b ^ 1), ((j - 1) >> 1) & 1))
+                timed_out = true;
+            if (gate && j >= 1 && j + 1 < nch && !timed_out) {
+                ++n_g[b ^ 1];
                 tc::mbar_arrive_expect_tx(bar_g + (b ^ 1), Cfg::G_TILE);
                 tc::tma_load_2d(g_buf(b ^ 1), &tm_g, h * D + NE * r, t_begin + C * (j + 1), bar_g + (b ^ 1));
             }
@@ -1203,10 +1243,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     for (int p = 1; p < R; ++p) wait_cl(bar_free + b * R + (r + p) % R, ((j - 2) >> 1) & 1);
                 }
                 const float own = s_rowpart[(b * 2) * C + t] + s_rowpart[(b * 2 + 1) * C + t];
+                if (!xdead) {
 #pragma unroll
-                for (int p = 1; p < R; ++p)
-                    st_async_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own,
-                                 cluster_map(bar_full + b, (r + p) % R));
+                    for (int p = 1; p < R; ++p)
+                        st_async_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own,
+                                     cluster_map(bar_full + b, (r + p) % R));
+                }
             }
             // the outputs of chunk j - 1 (read before the __syncthreads above) are out:
             // each peer may overwrite s_rowsq[(j - 1) & 1] with its sums of chunk j + 1
@@ -1268,8 +1310,17 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 *reinterpret_cast<float4*>(dst + c + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
         }
     }
-    if (timed_out && w.err) atomicOr(w.err, 1);
-    drain_if(timed_out);
+    // give-up path: wait for the copies and tensor-core work thread 0 issued and
+    // for the peers' row sums of the phases it armed, before any of this CTA's
+    // shared memory or TMEM is released
+    if (__syncthreads_or(timed_out || xdead) && tid == 0) {
+        bool drained = tc::drain_phase(mbar, n_mma) & tc::drain_phase(bar_ck, n_ck) & tc::drain_phase(bar_rk, n_rk);
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+            drained = drained & tc::drain_phase(bar_aw + b, n_aw[b]) & tc::drain_phase(bar_g + b, n_g[b]) &
+                      tc::drain_phase(bar_full + b, n_full[b]);
+        atomicOr(w.err, drained ? tc::ERR_WAIT : tc::ERR_WAIT | tc::ERR_DRAIN);
+    }
     tc::fence_before_sync();
     __syncthreads();
     cluster_sync_all();   // no CTA leaves while a peer may still write to its shared memory
@@ -1345,6 +1396,7 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     w.gm = reinterpret_cast<float*>(recs + L.gm);
     w.nrec = L.nrec;
     w.zero_v = (scan_flags & KDA_SCAN_ZERO_V) ? 1 : 0;
+    w.wait_limit = wait_limit();
 
     const uint64_t rowq = (uint64_t)a.H * spl::D;
     const uint64_t rows = (uint64_t)a.T_total;
@@ -1369,7 +1421,7 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
 
     int launched = 0;
     if (parts & 1) {
-        spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base));
+        spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base), w.err);
         ++launched;
         if (L.nrec > 0) {
             const int nsm = spl::sm_count();

@@ -109,7 +109,7 @@ TC_DEV uint32_t sw128_bf16(int row, int col) {
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
-prefill_tc_kernel(kda_prefill_args a, int* err,
+prefill_tc_kernel(kda_prefill_args a, int* err, uint32_t wait_limit,
                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_g) {
@@ -158,6 +158,9 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     const uint32_t bytes_vg = gate ? 2 * BYTES_V : BYTES_V;
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, TM_COLS); tc::tmem_relinquish(); }
+    // thread 0 issues every copy and MMA; it counts the phases it issued on each
+    // mbarrier, for the give-up path at the end
+    uint32_t n_in = 0, n_vg = 0, n_mma = 0;
     if (tid == 0) {
         tc::mbar_init(mbar, 1);
         tc::mbar_init(bar_in, 1);
@@ -176,6 +179,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
             tc::mbar_arrive_expect_tx(bar_vg, bytes_vg);
             tc::tma_load_2d(sm + OFF_RAWV, &tm_v, h * D + NE * r, t_begin, bar_vg);
             if (gate) tc::tma_load_2d(sm + OFF_RAWG, &tm_g, h * D + NE * r, t_begin, bar_vg);
+            n_in = n_vg = 1;
         }
     }
     tc::fence_before_sync();
@@ -185,9 +189,16 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int c_lo = hf * (NE / 2);    // this thread's half of a 64-column TMEM region
     uint32_t ph_mma = 0, ph_in = 0, ph_vg = 0;
+    // A wait that gives up records it; this thread then skips every later wait,
+    // and thread 0 issues no further copy or MMA, so the kernel runs to its end
+    // (its results are invalid) and drains what was issued.  The cluster
+    // barriers are unconditional, so the peer CTA is never left waiting.
     bool timed_out = false;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (!timed_out && !tc::mbar_wait_bounded(bar, parity, wait_limit)) timed_out = true;
+    };
     auto mma_wait = [&]() {
-        if (!tc::mbar_wait_bounded(mbar, ph_mma, 1u << 22)) timed_out = true;
+        wait(mbar, ph_mma);
         ph_mma ^= 1u;
         tc::fence_after_sync();
     };
@@ -224,7 +235,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
             s_beta[tid] = beta_next;
             beta_next = (c0 + C + tid < t_end) ? a.beta[(size_t)(c0 + C + tid) * H + h] : 0.f;
         }
-        if (!tc::mbar_wait_bounded(bar_in, ph_in, 1u << 22)) timed_out = true;
+        wait(bar_in, ph_in);
         ph_in ^= 1u;
 
         // ---- 1a. q/k L2 norms (warp w: tokens 8w..8w+7) from the staged tiles
@@ -514,7 +525,7 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
             }
         }
         __syncthreads();   // Gram tiles are dead from here on
-        if (!tc::mbar_wait_bounded(bar_vg, ph_vg, 1u << 22)) timed_out = true;
+        wait(bar_vg, ph_vg);
         ph_vg ^= 1u;
 
         // ---- 4. B_pre = [V_half | Gamma K]^T (smem) and A3 = (K gamma_C / Gamma)^T (TMEM)
@@ -559,7 +570,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         __syncthreads();
 
         // ---- 5. MMA 1: D[:, 0:192] = [T beta ; P] . [V_half | Gamma K]
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
+            ++n_mma;
             tc::fence_after_sync();
             const uint32_t bb = tc::smem_u32(sBpre);
 #pragma unroll
@@ -570,7 +582,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         mma_wait();
         // region RB is free again: fetch the next chunk's q, k, z into it
-        if (tid == 0 && has_next) {
+        if (tid == 0 && has_next && !timed_out) {
+            ++n_in;
             tc::fence_proxy_async();
             tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
             tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, h * D, c0 + C, bar_in);
@@ -613,7 +626,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         __syncthreads();
 
         // ---- 7. MMA 2: [V' ; O] = [U ; U_o] + A1 . S
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
+            ++n_mma;
             tc::fence_after_sync();
             const uint32_t sb = tc::smem_u32(sSop);
 #pragma unroll
@@ -689,7 +703,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
         __syncthreads();
         // v and g_in of this chunk are consumed: fetch the next chunk's
-        if (tid == 0 && has_next) {
+        if (tid == 0 && has_next && !timed_out) {
+            ++n_vg;
             tc::fence_proxy_async();
             tc::mbar_arrive_expect_tx(bar_vg, bytes_vg);
             tc::tma_load_2d(sm + OFF_RAWV, &tm_v, h * D + NE * r, c0 + C, bar_vg);
@@ -697,7 +712,8 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
         }
 
         // ---- 9. MMA 3: dS = (K gamma_C / Gamma)^T . V'
-        if (tid == 0) {
+        if (tid == 0 && !timed_out) {
+            ++n_mma;
             tc::fence_after_sync();
             const uint32_t vb = tc::smem_u32(sVop);
 #pragma unroll
@@ -758,7 +774,13 @@ prefill_tc_kernel(kda_prefill_args a, int* err,
                 *reinterpret_cast<float4*>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
     }
-    if (timed_out && err) atomicOr(err, 1);
+    // give-up path: wait for the copies and MMAs thread 0 issued before any of
+    // this CTA's shared memory or TMEM is released
+    if (__syncthreads_or(timed_out) && tid == 0) {
+        const bool drained = tc::drain_phase(bar_in, n_in) & tc::drain_phase(bar_vg, n_vg) &
+                             tc::drain_phase(mbar, n_mma);
+        atomicOr(err, drained ? tc::ERR_WAIT : tc::ERR_WAIT | tc::ERR_DRAIN);
+    }
     tc::fence_before_sync();
     __syncthreads();
     cluster_sync_all();   // no CTA leaves while its peer may still write to its shared memory
@@ -797,9 +819,11 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s) {
                            CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, row, rows, tcp::NE,
                            tcp::C, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    // the call's error word starts clear (the kernel sets it when a wait gives up)
+    if ((e = cudaMemsetAsync(a.workspace, 0, sizeof(int), s)) != cudaSuccess) return e;
     dim3 grid(2, a.H, a.num_seqs);
     tcp::prefill_tc_kernel<<<grid, tcp::NT, tcp::SMEM_BYTES, s>>>(a, reinterpret_cast<int*>(a.workspace),
-                                                                  mq, mk, mz, mv, mg);
+                                                                  wait_limit(), mq, mk, mz, mv, mg);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -812,24 +836,17 @@ cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device with that device current (in host code the symbol name is only a
-// host-side stand-in, never a device address).
-static cudaError_t noalloc_scratch_address(void** out) {
-    static std::mutex mu;
-    static void* addr[256] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// symbol's name is only a host-side stand-in, never a device address, so it is
+// looked up with that device current -- on every call: the lookup allocates
+// nothing, and an address cached across calls would go stale if the device's
+// context were reset and the library's module loaded again.  The first lookup
+// on a device loads the module there.
+cudaError_t noalloc_scratch_address(void** out) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = p;
-    }
-    *out = addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -841,10 +858,8 @@ cudaError_t launch_prefill_tc_noalloc(const kda_prefill_args& a, cudaStream_t s)
     void* scratch = nullptr;
     cudaError_t e = noalloc_scratch_address(&scratch);
     if (e != cudaSuccess) return e;
-    const size_t need = prefill_tc_workspace_size(a);
-    // the error word must start at zero; the array keeps the previous call's contents
-    e = cudaMemsetAsync(scratch, 0, need, s);
-    if (e != cudaSuccess) return e;
+    // the array keeps the previous call's contents; the launch below clears the
+    // error word, the only part of it that must start at zero
     kda_prefill_args b = a;
     b.workspace = scratch;
     b.workspace_bytes = KDA_NOALLOC_SCRATCH_BYTES;

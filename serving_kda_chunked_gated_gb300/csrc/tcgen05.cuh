@@ -145,6 +145,24 @@ TC_DEV bool mbar_wait_bounded(uint64_t* mbar, uint32_t parity, uint32_t limit = 
     return false;
 }
 
+// Default bound of a wait, in polls (seconds at most); kernels take the bound
+// of their waits on local copies and tensor-core work as a launch parameter.
+constexpr uint32_t WAIT_POLLS = 1u << 22;
+
+// The give-up path of a kernel whose bounded wait ran out: the thread that
+// issues asynchronous copies and tensor-core work stops issuing, and before
+// the CTA releases its shared memory and TMEM it waits here for the last phase
+// it issued on each mbarrier (n_issued phases so far; phases complete in order
+// and the kernels keep at most one outstanding per mbarrier, so the last
+// phase's parity identifies it).  Returns false if that wait ran out too.
+TC_DEV bool drain_phase(uint64_t* mbar, uint32_t n_issued) {
+    return n_issued == 0 || mbar_wait_bounded(mbar, (n_issued - 1) & 1u, WAIT_POLLS);
+}
+
+// Error word bits set by a kernel whose bounded wait ran out
+constexpr int ERR_WAIT = 1;    // a wait gave up: the call's outputs are invalid
+constexpr int ERR_DRAIN = 2;   // and the wait for work already issued gave up as well
+
 // expect `bytes` more transaction bytes on the mbarrier and arrive once
 TC_DEV void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"

@@ -19,13 +19,15 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 KDA_BF16, KDA_F32 = 0, 1
 STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_SHAPE", 3: "KDA_ERR_DTYPE",
           4: "KDA_ERR_ALIGN", 5: "KDA_ERR_SEQLENS", 6: "KDA_ERR_UNSUPPORTED",
-          7: "KDA_ERR_CUDA", 8: "KDA_ERR_WORKSPACE"}
+          7: "KDA_ERR_CUDA", 8: "KDA_ERR_WORKSPACE", 9: "KDA_ERR_TIMEOUT"}
+KDA_OK, KDA_ERR_TIMEOUT = 0, 9
+WAIT_LIMIT_DEFAULT = 0xFFFFFFFF
 
 EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size",
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
             "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count",
             "kda_short_conv", "kda_short_conv_step", "kda_kcp_apply", "kda_prefill_records",
-            "kda_prefill_scan"]
+            "kda_prefill_scan", "kda_get_last_device_error", "kda_debug_set_wait_limit"]
 
 _vp = ctypes.c_void_p
 
@@ -125,6 +127,10 @@ def load_library(path: str = LIB_PATH):
     lib.kda_last_error_string.restype = ctypes.c_char_p
     lib.kda_version.restype = ctypes.c_char_p
     lib.kda_launch_count.restype = ctypes.c_uint64
+    lib.kda_get_last_device_error.argtypes = [_vp, _vp]
+    lib.kda_get_last_device_error.restype = ctypes.c_int
+    lib.kda_debug_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.kda_debug_set_wait_limit.restype = ctypes.c_uint32
     _lib = lib
     return lib
 
@@ -132,6 +138,25 @@ def load_library(path: str = LIB_PATH):
 def launch_count() -> int:
     """Kernel launches enqueued by this library from the calling thread so far."""
     return int(load_library().kda_launch_count())
+
+
+def device_error(workspace=None, stream=None) -> int:
+    """``kda_get_last_device_error``: waits for ``stream``, then reads and clears
+    the error word of ``workspace`` (a prefill workspace tensor), or of the
+    array ``kda_prefill_noalloc`` uses when ``workspace`` is None.  Returns
+    KDA_OK (0) or KDA_ERR_TIMEOUT (9); raises on any other status."""
+    st = load_library().kda_get_last_device_error(_p(workspace), _stream(stream))
+    if st not in (KDA_OK, KDA_ERR_TIMEOUT):
+        _check(st, "kda_get_last_device_error")
+    return st
+
+
+def set_wait_limit(polls: int) -> int:
+    """``kda_debug_set_wait_limit`` (test hook): the poll bound of the prefill
+    kernels' waits on copies and MMAs for later launches; WAIT_LIMIT_DEFAULT
+    restores the default, 0 makes every such wait give up at once.  Returns the
+    previous setting."""
+    return int(load_library().kda_debug_set_wait_limit(ctypes.c_uint32(polls)))
 
 
 def _check(status: int, what: str):
@@ -207,6 +232,18 @@ def prefill_raw(args: PrefillArgs, stream=None, recurrent: bool = False):
 
 PREFILL_MIN_WORKSPACE = 256   # smallest workspace of the tensor-core path (single-pass schedule)
 _WS_CACHE = {}                # prefill(workspace="cache"): one buffer per device
+
+
+def cached_workspace(dev):
+    """The buffer ``prefill(workspace="cache")`` uses on ``dev`` (None before the
+    first such call)."""
+    dev = torch.device(dev)
+    return _WS_CACHE.get((dev.type, dev.index if dev.index is not None else torch.cuda.current_device()))
+
+
+def release_workspace_cache():
+    """Drop the cached workspaces (their memory returns to torch's allocator)."""
+    _WS_CACHE.clear()
 
 
 def prefill_from_host(q, k, v, z, beta, A, S0=None, g_in=None, norm_w=None, out=None, slab=16384,
@@ -356,7 +393,7 @@ def prefill(q, k, v, z, beta, A, cu_seqlens=None, S0=None, g_in=None, norm_w=Non
                     _WS_CACHE[key] = ws = torch.empty(need, dtype=torch.uint8, device=dev)
                 workspace = ws
             elif workspace is None:
-                workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
             args.workspace = workspace.data_ptr()
             args.workspace_bytes = workspace.numel() * workspace.element_size()
     prefill_raw(args, stream=stream, recurrent=recurrent)
@@ -389,7 +426,6 @@ def prefill_records(q, k, v, z, beta, A, cu_seqlens=None, g_min=-5.0, qk_l2norm=
                              qk_l2norm=qk_l2norm, gate=gate)
     need = prefill_workspace_size(args)
     ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    ws[:4].zero_()
     args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
     _check(load_library().kda_prefill_records(ctypes.byref(args), _stream(stream)), "kda_prefill_records")
     return Records(args, (q, k, v, z, beta, A, cu_seqlens, cu_host), ws, (T, H, dk, v.shape[2], cu_host.numel() - 1))
