@@ -83,3 +83,30 @@ def test_decode_y_only(kda_lib, cuda_dev):
     _, _, ry = oracle.decode_step(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"],
                                   d["state"], g_in=f64(d, "g_in"))
     assert rel(host(y), ry) < TOL_O
+
+
+def test_decode_normalises_raw_q_k(kda_lib, cuda_dev):
+    """q and k NOT normalised (each token-head vector scaled by a factor in
+    0.2..5) with qk_l2norm on: the kernel's own L2 norm of q and k matches the
+    oracle's, element by element on the state."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    from kda_testutil import parity
+    d = I.make_decode(I.workload("decode_256", H=4, B=16))
+    rng = np.random.default_rng(3)
+    for key in ("q", "k"):
+        f = rng.uniform(0.2, 5.0, size=(16, 4, 1)).astype(np.float32)
+        d[key] = I.bf16_bits(I.bf16_to_f32(d[key]) * f)
+    o, y, st = _run(kda, d, cuda_dev)
+    ro, rs, ry = oracle.decode_step(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"],
+                                    d["state"], g_in=f64(d, "g_in"), qk_l2norm=True)
+    parity("o", host(o), ro, TOL_O, bf16_out=True)
+    parity("y", host(y), ry, TOL_O, bf16_out=True, floor_ref=ro)
+    parity("state", host(st), rs, TOL_S)
+    np.testing.assert_allclose(host(st), rs, rtol=0, atol=2e-5)
+    # without the norm the same inputs give a different result: the flag is read
+    st2 = to_dev(d["state"].copy(), cuda_dev)
+    o2, _ = kda.decode_step(to_dev(d["q"], cuda_dev, True), to_dev(d["k"], cuda_dev, True),
+                            to_dev(d["v"], cuda_dev, True), to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev),
+                            to_dev(d["A"], cuda_dev), st2, qk_l2norm=False)
+    torch.cuda.synchronize()
+    assert rel(host(o2), ro) > 0.1

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from serving_kda_chunked_gated_gb300 import inputs as I
-from kda_testutil import TOL_O, TOL_S, f64, host, qkv_to_dev, rel, to_dev
+from kda_testutil import TOL_O, TOL_S, f64, host, parity, qkv_to_dev, rel, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -31,15 +31,13 @@ def run_oracle(d, gate=None, s0=True):
                           cu_seqlens=d["cu_seqlens"], S0=d["S0"] if s0 else None, g_in=g)
 
 
-def check(res, ref, tol_o=TOL_O, tol_s=TOL_S):
+def check(res, ref, tol_o=TOL_O, tol_s=TOL_S, bf16=True, seq_bounds=None):
     o, S_T, y = res
     ro, rS, ry = ref
-    eo, es = rel(host(o), ro), rel(host(S_T), rS)
-    assert eo < tol_o, f"o rel-L2 {eo:.3e}"
-    assert es < tol_s, f"S_T rel-L2 {es:.3e}"
+    parity("o", host(o), ro, tol_o, bf16_out=bf16 and o.dtype == torch.bfloat16, seq_bounds=seq_bounds)
+    parity("S_T", host(S_T), rS, tol_s)
     if ry is not None:
-        ey = rel(host(y), ry)
-        assert ey < tol_o, f"y rel-L2 {ey:.3e}"
+        parity("y", host(y), ry, tol_o, bf16_out=True, seq_bounds=seq_bounds, floor_ref=ro)
 
 
 def test_tiny_fp32(kda_lib, cuda_dev):
@@ -95,7 +93,7 @@ def test_schedules_agree(kda_lib, cuda_dev, cu):
     for name, ws in (("split", ws_full), ("single", ws_min)):
         res[name] = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
         torch.cuda.synchronize()
-        assert int(ws[:4].view(torch.int32).item()) == 0, name
+        assert kda.device_error(ws) == kda.KDA_OK, name
     ref = run_oracle(d)
     for name in res:
         check(res[name], ref)
@@ -125,22 +123,26 @@ def test_adversarial_gates(kda_lib, cuda_dev):
 
 
 def test_full_prefill_8k_sampled(kda_lib, cuda_dev):
-    """Full 8192-token, 32-head prefill; the oracle recomputes two heads."""
+    """Full 8192-token, 32-head prefill (the prefill_8k workload, chunk-parallel
+    schedule); the oracle recomputes three heads."""
     import serving_kda_chunked_gated_gb300.kda as kda
     w = I.workload("prefill_8k")
     d = I.make_prefill(w)
     o, S_T, _ = run_gpu(kda, d, cuda_dev)
-    heads = [0, 31]
+    heads = [0, 13, 31]
     ds = I.make_prefill(w, heads=heads)
     ro, rS, _ = run_oracle(ds)
-    assert rel(host(o)[:, heads], ro) < TOL_O
-    assert rel(host(S_T)[:, heads], rS) < TOL_S
+    parity("o", host(o)[:, heads], ro, TOL_O, bf16_out=True)
+    parity("S_T", host(S_T)[:, heads], rS, TOL_S)
 
 
-def test_full_prefill_128k_sampled_and_deterministic(kda_lib, cuda_dev):
-    """Long-context prefill (131072 tokens, 32 heads, prefix state, fused gate):
-    one head checked against the oracle; two runs bit-identical; no bounded
-    wait gave up (the workspace error word stays 0)."""
+def test_prefill_128k_bench_config(kda_lib, cuda_dev):
+    """The benchmark's headline workload exactly as it is timed: prefill_128k
+    (131072 tokens, 32 heads, prefix state S0 ~ N(0, 0.02), fused output gate),
+    a full workspace, so the chunk-parallel schedule runs.  o, y and S_T of four
+    heads (first and last among them) against the oracle, row by row; two runs
+    bit-identical; no bounded wait gave up.  The same inputs through the
+    single-pass schedule (minimal workspace) agree with it and with the oracle."""
     import serving_kda_chunked_gated_gb300.kda as kda
     w = I.workload("prefill_128k")
     d = I.make_prefill(w)
@@ -148,34 +150,45 @@ def test_full_prefill_128k_sampled_and_deterministic(kda_lib, cuda_dev):
     args = dict(cu_seqlens=to_dev(d["cu_seqlens"], cuda_dev), S0=to_dev(d["S0"], cuda_dev),
                 g_in=to_dev(d["g_in"], cuda_dev, True))
     z, beta, A = to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev), to_dev(d["A"], cuda_dev)
-    ws = torch.zeros(4096, dtype=torch.uint8, device=cuda_dev)
-    o, S_T, y = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
-    o2, S_T2, y2 = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
+    del d
+    o, S_T, y = kda.prefill(q, k, v, z, beta, A, workspace="cache", **args)
+    o2, S_T2, y2 = kda.prefill(q, k, v, z, beta, A, workspace="cache", **args)
     torch.cuda.synchronize()
-    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert kda.device_error(kda.cached_workspace(cuda_dev)) == 0
     assert torch.equal(o, o2) and torch.equal(S_T, S_T2) and torch.equal(y, y2)
+    del o2, S_T2, y2
+    kda.release_workspace_cache()
+    ws = torch.zeros(4096, dtype=torch.uint8, device=cuda_dev)
+    o_sp, S_sp, y_sp = kda.prefill(q, k, v, z, beta, A, workspace=ws, **args)
+    torch.cuda.synchronize()
+    assert kda.device_error(ws) == 0
     del q, k, v, z, beta, args
-    heads = [5]
+    heads = [0, 5, 17, 31]
     ds = I.make_prefill(w, heads=heads)
     ro, rS, ry = run_oracle(ds)
-    assert rel(host(o[:, heads]), ro) < TOL_O
-    assert rel(host(y[:, heads]), ry) < TOL_O
-    assert rel(host(S_T[:, heads]), rS) < TOL_S
+    parity("o", host(o[:, heads]), ro, TOL_O, bf16_out=True)
+    parity("y", host(y[:, heads]), ry, TOL_O, bf16_out=True, floor_ref=ro)
+    parity("S_T", host(S_T[:, heads]), rS, TOL_S)
+    parity("o single-pass", host(o_sp[:, heads[:2]]), ro[:, :2], TOL_O, bf16_out=True)
+    parity("S_T single-pass", host(S_sp[:, heads[:2]]), rS[:, :2], TOL_S)
+    assert rel(host(o_sp), host(o)) < TOL_O and rel(host(y_sp), host(y)) < TOL_O
+    assert rel(host(S_sp), host(S_T)) < TOL_S
 
 
 def test_full_varlen_16_sampled(kda_lib, cuda_dev):
-    """Packed 16-sequence prefill (lengths 512..16384); two heads checked for
-    every sequence; the packed result equals per-sequence calls bit for bit."""
+    """Packed 16-sequence prefill (lengths 512..16384); three heads checked,
+    every sequence on its own; the packed result equals per-sequence calls bit
+    for bit."""
     import serving_kda_chunked_gated_gb300.kda as kda
     w = I.workload("varlen_16")
     d = I.make_prefill(w)
     o, S_T, _ = run_gpu(kda, d, cuda_dev)
-    heads = [0, 31]
+    heads = [0, 16, 31]
     ds = I.make_prefill(w, heads=heads)
     ro, rS, _ = run_oracle(ds)
-    assert rel(host(o)[:, heads], ro) < TOL_O
-    assert rel(host(S_T)[:, heads], rS) < TOL_S
     cu = d["cu_seqlens"]
+    parity("o", host(o)[:, heads], ro, TOL_O, bf16_out=True, seq_bounds=cu)
+    parity("S_T", host(S_T)[:, heads], rS, TOL_S, seq_bounds=range(len(cu)))
     for n in (0, 7, 15):
         s, e = int(cu[n]), int(cu[n + 1])
         sub = dict(d)
