@@ -183,6 +183,51 @@ def nbytes(t):
     return 0 if t is None else t.numel() * t.element_size()
 
 
+def prefill_alg_bytes(wl, T, N):
+    """Algorithmic bytes of one prefill call: q, k, v (bf16), z (fp32), beta,
+    o (bf16) [+ g_in, y (bf16)] per token and head, plus S_T [+ S0] (fp32)."""
+    H, d = wl["H"], wl["d"]
+    io_per_tok_head = 3 * 2 * d + 4 * d + 4 + 2 * d + (2 * 2 * d if wl["gate"] else 0)
+    return T * H * io_per_tok_head + N * H * d * d * 4 * (2 if wl["S0"] else 1)
+
+
+def time_prefill_workload(torch, kda, name, dev, seed, steps, warmup, pk):
+    """Throughput line of another prefill workload, timed like the headline
+    (inputs resident, CUDA events around `steps` back-to-back calls)."""
+    wl = WORKLOADS[name]
+    H, d = wl["H"], wl["d"]
+    inp, T, N = make_prefill_inputs(torch, wl, dev, seed=seed)
+    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(o) if inp["g_in"] is not None else None
+    S_T = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    cu_host = inp["cu_seqlens"].cpu()
+    pa = kda.make_prefill_args(inp["q"], inp["k"], inp["v"], inp["z"], inp["beta"], inp["A"],
+                               inp["cu_seqlens"], cu_host, o, S0=inp["S0"], S_T=S_T, g_in=inp["g_in"], y=y)
+    ws_bytes = kda.prefill_workspace_size(pa)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    pa.workspace, pa.workspace_bytes = ws.data_ptr(), ws_bytes
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        kda.prefill_raw(pa, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        kda.prefill_raw(pa, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    err = kda.device_error(ws)
+    alg = prefill_alg_bytes(wl, T, N)
+    achieved = alg / (ms * 1e-3) / 1e9
+    flops = T * H * FLOP_PER_TOKEN_HEAD
+    return {"workload": name, "tokens": T, "num_seqs": N, "ms_per_step": ms, "value": T / (ms * 1e-3),
+            "unit": "tokens/s", "device_error": kda.STATUS.get(err, err),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm"], "algorithmic_bytes_per_launch": alg,
+                         "tensor_frac_of_bf16": flops / (ms * 1e-3) / 1e12 / pk["bf16"]}}
+
+
 def kernel_traffic(kernel_file, name, field="bytes_per_launch"):
     """A field of the committed ncu summary (DRAM bytes per launch by default),
     if the kernel source still matches the hash recorded with it (else None)."""
@@ -256,24 +301,37 @@ def run_ours(args, rank, world):
     ms = e0.elapsed_time(e1) / args.steps
     ms_all = max_over_ranks(ms, dev)
 
-    # ---- decode step (secondary): state read + written once per step
+    headline_err = kda.device_error(ws)
+
+    # ---- the other prefill workloads (secondaries): prefill_8k, varlen_16
+    others = {}
+    if args.workload == "prefill_128k" and not args.no_secondaries:
+        for name in ("prefill_8k", "varlen_16"):
+            others[name] = time_prefill_workload(torch, kda, name, dev, 2000 + rank, args.steps,
+                                                 max(args.warmup, 3), pk)
+            torch.cuda.empty_cache()
+
+    # ---- decode step (secondary): state read + written once per step; two state
+    # pools (512 MiB each) alternate, so a step never finds its state in L2
     dec = make_decode_inputs(torch, dev, seed=99 + rank)
     Nd = dec["q"].shape[0]
     od = torch.empty((Nd, H, d), dtype=torch.bfloat16, device=dev)
     yd = torch.empty_like(od)
-    da = kda.make_decode_args(dec["q"], dec["k"], dec["v"], dec["z"], dec["beta"], dec["A"],
-                              dec["state"], o=od, y=yd, g_in=dec["g_in"])
-    for _ in range(max(args.warmup, 3)):
-        kda.decode_step_raw(da, stream)
+    state2 = dec["state"].clone()
+    das = [kda.make_decode_args(dec["q"], dec["k"], dec["v"], dec["z"], dec["beta"], dec["A"],
+                                st, o=od, y=yd, g_in=dec["g_in"]) for st in (dec["state"], state2)]
+    for i in range(max(args.warmup, 3)):
+        kda.decode_step_raw(das[i & 1], stream)
     dsteps = max(args.steps, 20) * 4
     torch.cuda.synchronize()
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d0.record(stream)
-    for _ in range(dsteps):
-        kda.decode_step_raw(da, stream)
+    for i in range(dsteps):
+        kda.decode_step_raw(das[i & 1], stream)
     d1.record(stream)
     torch.cuda.synchronize()
     dec_ms = d0.elapsed_time(d1) / dsteps
+    del state2
 
     # ---- prefix-cache snapshots (secondary): the same prefill writing the state
     # every SNAP_INTERVAL tokens of each sequence
@@ -421,8 +479,7 @@ def run_ours(args, rank, world):
         return None
 
     # algorithmic bytes of one prefill launch
-    io_per_tok_head = 3 * 2 * d + 4 * d + 4 + 2 * d + (2 * 2 * d if wl["gate"] else 0)
-    alg_bytes = T * H * io_per_tok_head + N * H * d * d * 4 * (2 if wl["S0"] else 1)
+    alg_bytes = prefill_alg_bytes(wl, T, N)
     alg_flops = T * H * FLOP_PER_TOKEN_HEAD
     achieved = alg_bytes / (ms * 1e-3) / 1e9
     tf32_peak = pk["bf16"] * TF32_OVER_BF16
@@ -456,7 +513,10 @@ def run_ours(args, rank, world):
                                 "peak_tf32_tflops": tf32_peak,
                                 "frac_of_tf32": alg_flops / (ms * 1e-3) / 1e12 / tf32_peak,
                                 "frac_of_bf16": alg_flops / (ms * 1e-3) / 1e12 / pk["bf16"]}},
+        "device_error": kda.STATUS.get(headline_err, headline_err),
+        "workloads": others or None,
         "decode": {"workload": "decode_256", "ms_per_step": dec_ms, "value": dec_gbs, "unit": "GB/s",
+                   "state_pools": "two 512 MiB pools alternate between steps",
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": pk["hbm"], "unit": "GB/s",
                                 "frac": dec_gbs / pk["hbm"],
                                 "traffic": kernel_traffic("decode.cu", "decode"),
@@ -556,6 +616,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill_128k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondaries", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -94,10 +94,9 @@ typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
  *   norm_w [dv] float32 RMSNorm weight, or NULL (ones); used with g_in
  *   y     [T_total, H, dv]   bf16 fused output gate result (required iff g_in)
  *
- * Supported: dk = dv = 128 with bf16 q/k/v (tensor-core chunked path), and
- * dk = dv in {32, 64, 128} with float32 q/k/v (CUDA-core path); H >= 1.
- * workspace: device scratch.  On the tensor-core path the size selects the
- * schedule:
+ * Supported: dk = dv = 128 with bf16 q/k/v, and dk = dv in {32, 64, 128} with
+ * float32 q/k/v; H >= 1.  workspace: device scratch; its size selects the
+ * schedule.  bf16, d = 128 (the tensor-core path):
  *  - workspace_bytes >= kda_prefill_workspace_size(): chunk-parallel schedule
  *    (one pass over all (chunk, head) pairs in parallel writes each chunk's
  *    state-free terms, 160.5 KiB per chunk and head, to the workspace; a second
@@ -106,12 +105,16 @@ typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
  *    (one cluster per (sequence, head) walks its chunks); no scratch beyond
  *    the error word.
  *  - less: KDA_ERR_WORKSPACE.
+ * float32, d = 32 or 64: with kda_prefill_workspace_size() bytes the same
+ * chunk-parallel schedule (tensor cores, the channels d..127 taken as zero,
+ * which leaves every result exact); with less (NULL included) the per-token
+ * recurrence on CUDA cores.  float32, d = 128: the per-token recurrence.
  * The first 4 bytes of the workspace are the call's error word: kda_prefill
  * and kda_prefill_records clear it on the stream before their kernels run,
  * kda_prefill_scan does not (a records call's word stays visible through its
  * scans), and a bounded wait inside a kernel that gives up sets it; read it
- * with kda_get_last_device_error.  The CUDA-core path needs no workspace
- * (size 0; may be NULL) and has no waits.
+ * with kda_get_last_device_error.  The per-token CUDA-core path needs no
+ * workspace (may be NULL) and has no waits.
  */
 #define KDA_PREFILL_MIN_WORKSPACE 256
 typedef struct {
@@ -174,8 +177,8 @@ kda_status kda_prefill(const kda_prefill_args* args, void* stream);
  *   args->workspace, which must hold kda_prefill_workspace_size(args) bytes
  *   (else KDA_ERR_WORKSPACE).  S0, S_T, o, g_in, norm_w, y and the snapshot
  *   fields are not read.  Inputs and their validation as for kda_prefill;
- *   KDA_ERR_UNSUPPORTED where kda_prefill would not take the chunk-parallel
- *   schedule (inputs other than bf16 q/k/v with d_k = d_v = 128).
+ *   KDA_ERR_UNSUPPORTED for inputs the chunk-parallel schedule does not take
+ *   (other than bf16 q/k/v with d = 128 or float32 q/k/v with d = 32, 64).
  * kda_prefill_scan: the state recurrence over the records that
  *   kda_prefill_records wrote into args->workspace, producing o, S_T, y and
  *   snapshots exactly as kda_prefill (bit for bit) from args->S0.  The record

@@ -20,6 +20,7 @@ cudaError_t launch_prefill_tc_noalloc(const kda_prefill_args& a, cudaStream_t s)
 size_t prefill_tc_workspace_size(const kda_prefill_args& a);
 cudaError_t launch_prefill_tc(const kda_prefill_args& a, cudaStream_t s);
 size_t prefill_split_workspace_size(const kda_prefill_args& a);
+bool prefill_split_supported(const kda_prefill_args& a);
 cudaError_t launch_prefill_split(const kda_prefill_args& a, cudaStream_t s);
 cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int scan_flags, cudaStream_t s);
 cudaError_t launch_short_conv(const kda_short_conv_args& a, cudaStream_t s);
@@ -130,7 +131,7 @@ long kda_prefill_snapshot_count(const kda_prefill_args* a) {
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
     if (validate_prefill(a) != KDA_OK) return 0;
-    if (kda::prefill_tc_supported(*a)) return kda::prefill_split_workspace_size(*a);
+    if (kda::prefill_split_supported(*a)) return kda::prefill_split_workspace_size(*a);
     return 0;
 }
 
@@ -140,7 +141,7 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
     if (a->num_seqs == 0) return KDA_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (kda::prefill_tc_supported(*a)) {
+    if (kda::prefill_tc_supported(*a)) {          // bf16, d = 128: the workspace picks the schedule
         if (!a->workspace || a->workspace_bytes < KDA_PREFILL_MIN_WORKSPACE) return KDA_ERR_WORKSPACE;
         if (misaligned(a->workspace)) return KDA_ERR_ALIGN;
         if (a->workspace_bytes >= kda::prefill_split_workspace_size(*a))
@@ -149,8 +150,13 @@ kda_status kda_prefill(const kda_prefill_args* a, void* stream) {
             return KDA_ERR_UNSUPPORTED;   // the single-pass schedule relies on the bounded gate
         else
             e = kda::launch_prefill_tc(*a, s);
+    } else if (kda::prefill_split_supported(*a) && a->workspace &&
+               a->workspace_bytes >= kda::prefill_split_workspace_size(*a)) {
+        // float32, d = 32 or 64, with the chunk-parallel workspace: the chunked form
+        if (misaligned(a->workspace)) return KDA_ERR_ALIGN;
+        e = kda::launch_prefill_split(*a, s);
     } else {
-        e = kda::launch_prefill_recurrent(*a, s);
+        e = kda::launch_prefill_recurrent(*a, s);   // the per-token recurrence on CUDA cores
     }
     return e == cudaSuccess ? KDA_OK : cuda_fail(e);
 }
@@ -160,7 +166,7 @@ static kda_status prefill_split_part(const kda_prefill_args* a, int parts, int f
     kda_status st = validate_prefill(a);
     if (st != KDA_OK) return st;
     if (flags & ~KDA_SCAN_ZERO_V) return KDA_ERR_SHAPE;
-    if (!kda::prefill_tc_supported(*a)) return KDA_ERR_UNSUPPORTED;
+    if (!kda::prefill_split_supported(*a)) return KDA_ERR_UNSUPPORTED;
     if (a->num_seqs == 0) return KDA_OK;
     if (!a->workspace || a->workspace_bytes < kda::prefill_split_workspace_size(*a)) return KDA_ERR_WORKSPACE;
     if (misaligned(a->workspace)) return KDA_ERR_ALIGN;

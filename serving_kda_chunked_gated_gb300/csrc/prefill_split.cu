@@ -43,7 +43,6 @@ namespace spl {
 constexpr int C = 64;     // chunk length
 constexpr int D = 128;    // dk = dv
 constexpr int NT = 256;   // threads per CTA
-constexpr int QS = 132;   // padded row stride (floats) of the scaled q/k tiles
 constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
 constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
 constexpr int SCAN_R = 4; // scan: CTAs (value-column blocks) per (sequence, head)
@@ -174,19 +173,20 @@ TC_DEV float warp_reduce_scatter32(float (&v)[32], int lane) {
 // prep: the state-free part of every chunk
 // ---------------------------------------------------------------------------
 namespace prep {
-constexpr int RB_BYTES = 65536;                     // raw q,k,z | Gram tiles | [V | Gamma K]^T
-constexpr int TILE_BYTES = C * QS * 4;
+// Region RB, in turn: the raw q, k, z tiles; the Gram's B operand (the key versions);
+// the Gram tiles and the solve's scratch; B_pre = [V | Gamma K]^T.
+constexpr int KV_ROWS = 160;                        // key versions: 16 (a + 1) rows for a = 0..3
+constexpr int RB_BYTES = KV_ROWS * D * 4;           // 80 KB
 constexpr int OFF_RB = 0;
 constexpr int OFF_RAWQ = OFF_RB;                    // [C][D] bf16
 constexpr int OFF_RAWK = OFF_RB + C * D * 2;        // [C][D] bf16
 constexpr int OFF_RAWZ = OFF_RB + 2 * C * D * 2;    // [C][D] f32
+constexpr int OFF_KV = OFF_RB;                      // SW128 [160 rows][D]
 constexpr int OFF_AQK = OFF_RB;
 constexpr int OFF_AKK = OFF_RB + C * AS * 4;
 constexpr int OFF_BPRE = OFF_RB;                    // SW128 [256 rows][C]
-constexpr int OFF_QH = OFF_RB + RB_BYTES;
-constexpr int OFF_KR = OFF_QH + TILE_BYTES;
-constexpr int OFF_KH = OFF_KR + TILE_BYTES;
-constexpr int OFF_RAWV = OFF_KH + TILE_BYTES;       // two [C][64] bf16 tiles, 128-B swizzle
+constexpr int OFF_QK = OFF_RB + RB_BYTES;           // the Gram's A operand [Q~ ; K~], SW128 [128 rows][D]
+constexpr int OFF_RAWV = OFF_QK + 2 * C * D * 4;    // two [C][64] bf16 tiles, 128-B swizzle
 constexpr int OFF_SMALL = OFF_RAWV + 2 * C * 64 * 2;
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
@@ -196,21 +196,31 @@ constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_T
               SM_FLOATS = SM_LOC + 16;
 constexpr int EA_HEADS = 128;
 constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
-static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0, "swizzled tiles need 1024-B alignment");
+static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0 && OFF_QK % 1024 == 0 && OFF_KV % 1024 == 0,
+              "swizzled tiles need 1024-B alignment");
 static_assert(2 * D * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
 static_assert(3 * C * AS * 4 + (NT / 32) * 16 * 16 * 4 <= RB_BYTES, "region RB holds the solve tiles");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;
 constexpr uint32_t BYTES_V = C * D * 2;
+// float32 inputs with d_k = d_v = DIN <= 64: compact [C][DIN] fp32 tiles in the same
+// slots (q, k, z: 16 KB at most each, v: 16 KB at most); channels DIN..127 read as 0
+constexpr int DIN_MAX = 64;
 constexpr int NTP = 512;         // threads per CTA (16 warps; warps w, w+4, w+8, w+12 share TMEM lanes)
 constexpr uint32_t TM_D = 0;     // 256 cols: [U | W ; U_o | P Gamma K]
 constexpr uint32_t TM_A2 = 256;  // 64 cols: [T beta ; P beta]
+constexpr uint32_t TM_G = 320;   // 160 cols: [Q~ ; K~] . (key versions)^T
 constexpr uint32_t TM_COLS = 512;
+// first row of key version a (keys of sub-chunks 0..a referred to the start of sub-chunk a)
+__host__ __device__ constexpr int kv_row0(int a) { return 8 * a * (a + 1); }
 }  // namespace prep
 
 // GATE 0: K3's bounded gate; 1: Kimi Linear's Softplus gate, whose diagonal Gram
-// sub-blocks are formed pair by pair (their sub-chunk factors can exceed fp32)
-template <int GATE>
+// sub-blocks are formed pair by pair (their sub-chunk factors can exceed fp32).
+// IN32 0: bf16 q, k, v with d = 128; 1: float32 q, k, v with d = a.dk <= 64, the
+// channels from d to 127 taken as zero (every record term they touch is then 0, so
+// the d = 128 records and scan carry the smaller operator exactly).
+template <int GATE, int IN32>
 __global__ void __launch_bounds__(prep::NTP, 1)
 prep_kernel(kda_prefill_args a, Work w,
             const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -223,9 +233,28 @@ prep_kernel(kda_prefill_args a, Work w,
     const uint16_t* sRawK = reinterpret_cast<const uint16_t*>(sm + OFF_RAWK);
     const float* sRawZ = reinterpret_cast<const float*>(sm + OFF_RAWZ);
     const uint8_t* sRawV = sm + OFF_RAWV;
-    float* sQ = reinterpret_cast<float*>(sm + OFF_QH);
-    float* sKr = reinterpret_cast<float*>(sm + OFF_KR);
-    float* sK = reinterpret_cast<float*>(sm + OFF_KH);
+    const int din = IN32 ? a.dk : D;   // input channels
+    // raw input element (token t, channel d) of the staged tiles
+    auto raw_q = [&](int t, int d) -> float {
+        if (IN32) return d < din ? reinterpret_cast<const float*>(sRawQ)[t * din + d] : 0.f;
+        return bf16_to_f(sRawQ[t * D + d]);
+    };
+    auto raw_k = [&](int t, int d) -> float {
+        if (IN32) return d < din ? reinterpret_cast<const float*>(sRawK)[t * din + d] : 0.f;
+        return bf16_to_f(sRawK[t * D + d]);
+    };
+    auto raw_z = [&](int t, int d) -> float {
+        if (IN32) return d < din ? sRawZ[t * din + d] : 0.f;
+        return sRawZ[t * D + d];
+    };
+    auto raw_v = [&](int t, int e) -> float {
+        if (IN32) return e < din ? reinterpret_cast<const float*>(sRawV)[t * din + e] : 0.f;
+        return bf16_to_f(*reinterpret_cast<const uint16_t*>(sRawV + (e >> 6) * (C * 128) + sw128_bf16(t, e & 63)));
+    };
+
+    uint8_t* sQK = sm + OFF_QK;   // [Q~ ; K~]: rows t = q_t exp(G_t - G_start), rows 64 + t = k_t exp(...)
+    uint8_t* sKV = sm + OFF_KV;   // key versions
+    auto qk_at = [&](int r, int d) -> float& { return *reinterpret_cast<float*>(sQK + tc::sw128_offset(r, d, 2 * C)); };
     float* sAqk = reinterpret_cast<float*>(sm + OFF_AQK);
     float* sAkk = reinterpret_cast<float*>(sm + OFF_AKK);
     float* fs = reinterpret_cast<float*>(sm + OFF_SMALL);
@@ -246,6 +275,19 @@ prep_kernel(kda_prefill_args a, Work w,
     uint64_t* bar_in = mbar + 1;
     uint64_t* bar_v = mbar + 2;
     uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(mbar + 3);
+    const uint32_t bytes_qkz = IN32 ? 3u * C * din * 4 : BYTES_QKZ;
+    const uint32_t bytes_v = IN32 ? (uint32_t)C * din * 4 : BYTES_V;
+    auto load_qkz = [&](const Loc& l) {   // thread 0
+        tc::mbar_arrive_expect_tx(bar_in, bytes_qkz);
+        tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, l.h * din, l.t0, bar_in);
+        tc::tma_load_2d(sm + OFF_RAWK, &tm_k, l.h * din, l.t0, bar_in);
+        tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, l.h * din, l.t0, bar_in);
+    };
+    auto load_v = [&](const Loc& l) {     // thread 0
+        tc::mbar_arrive_expect_tx(bar_v, bytes_v);
+        tc::tma_load_2d(sm + OFF_RAWV, &tm_v, l.h * din, l.t0, bar_v);
+        if (!IN32) tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, l.h * D + 64, l.t0, bar_v);
+    };
 
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -292,13 +334,8 @@ prep_kernel(kda_prefill_args a, Work w,
         tc::tma_prefetch_desc(&tm_z);
         tc::tma_prefetch_desc(&tm_v);
         if (rec < w.nrec) {
-            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
-            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, cur.h * D, cur.t0, bar_in);
-            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, cur.h * D, cur.t0, bar_in);
-            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, cur.h * D, cur.t0, bar_in);
-            tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
-            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, cur.h * D, cur.t0, bar_v);
-            tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, cur.h * D + 64, cur.t0, bar_v);
+            load_qkz(cur);
+            load_v(cur);
             n_in = n_v = 1;
         }
     }
@@ -338,7 +375,12 @@ prep_kernel(kda_prefill_args a, Work w,
             const int t = v & (C - 1);
             const uint16_t* rowp = (v < C ? sRawQ : sRawK) + t * D + half * (D / 2);
             float ssum = 0.f;
-            if (t < nc) {
+            if (IN32 && t < nc) {   // channels half * din/2 .. +din/2 of the fp32 row
+                for (int c = half * (din >> 1); c < (half + 1) * (din >> 1); ++c) {
+                    const float x = v < C ? raw_q(t, c) : raw_k(t, c);
+                    ssum = fmaf(x, x, ssum);
+                }
+            } else if (!IN32 && t < nc) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int c = (i + 2 * v + half) & 7;
@@ -356,7 +398,9 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
 
-        // ---- 1b. gate and sub-chunk-relative decay factors (thread: channel d, sub-chunk b)
+        // ---- 1b. gate and sub-chunk-relative decay factors (thread: channel d, sub-chunk b);
+        //          q~, k~ (tf32) into the Gram's A operand, k_t exp(G_end(b) - G_t) kept in kf2
+        float kf2[16];
         {
             const int d = tid & (D - 1);
 #pragma unroll 1
@@ -368,25 +412,25 @@ prep_kernel(kda_prefill_args a, Work w,
                     const int t = 16 * b + i;
                     float alpha = 1.f, q = 0.f, k = 0.f;
                     if (t < nc) {
-                        const float g = GATE ? log_decay_softplus(sRawZ[t * D + d], eA)
-                                             : log_decay(sRawZ[t * D + d], eA, a.g_min);
+                        const float g = GATE ? log_decay_softplus(raw_z(t, d), eA)
+                                             : log_decay(raw_z(t, d), eA, a.g_min);
                         alpha = __expf(g);
                         L += g;
-                        q = bf16_to_f(sRawQ[t * D + d]) * s_rq[t];
-                        k = bf16_to_f(sRawK[t * D + d]) * s_rk[t];
+                        q = raw_q(t, d) * s_rq[t];
+                        k = raw_k(t, d) * s_rk[t];
                     }
                     F1 *= alpha;                   // exp(G_t - G_start(b))
                     al[i] = alpha;
                     kv[i] = k;
                     qv[i] = q;
                     Lc[i] = L;                     // G_t - G_start(b), log domain
-                    sQ[t * QS + d] = q * F1;
-                    sKr[t * QS + d] = k * F1;
+                    qk_at(t, d) = tc::to_tf32(q * F1);
+                    qk_at(C + t, d) = tc::to_tf32(k * F1);
                 }
                 float F2 = 1.f;                    // exp(G_end(b) - G_t)
 #pragma unroll
                 for (int i = 15; i >= 0; --i) {
-                    sK[(16 * b + i) * QS + d] = kv[i] * F2;
+                    kf2[i] = kv[i] * F2;
                     F2 *= al[i];
                 }
                 s_tau[b * D + d] = F1;
@@ -446,113 +490,95 @@ prep_kernel(kda_prefill_args a, Work w,
         }
         __syncthreads();
 
-        // ---- 2. Gram sub-blocks, mma.sync tf32: blocks 0..9 of A_qk, 10..19 of A_kk.
-        //         Warp w forms block w whole and one K-quarter (w & 3) of block 16 + w/4;
-        //         the four quarters of blocks 16..19 are added in a fixed order.
+        // ---- 2. Gram sub-blocks on the tensor cores.  Block (a, b), b <= a, of A_qk and A_kk is
+        //         sum_d q~_i k_j c_ab[d] / k~_i k_j c_ab[d] with k_j = k exp(G_end(b) - G_j) and
+        //         c_ab = exp(G_start(a) - G_end(b)) (<= 1 for b < a; 1/tau_a < e^80 for b = a: the
+        //         dense diagonal sub-blocks of the bounded gate).  Key version a holds the keys of
+        //         sub-chunks 0..a times c_ab; one MMA, [Q~ ; K~] (128 rows) x versions (160 rows),
+        //         leaves every block in TMEM, and each row reads the version of its own sub-chunk.
         {
-            const int g = lane >> 2, t4 = lane & 3;
-            float* part = sAkk + C * AS;               // [16 warps][16][16] quarter-block partials
-            float acc[2][2][4];
+            const int d = tid & (D - 1), b = tid >> 7;
 #pragma unroll
-            for (int it = 0; it < 2; ++it)
+            for (int av = 0; av < 4; ++av) {
+                if (av < b) continue;
+                // the softplus gate's diagonal blocks come pair by pair (their factor can overflow)
+                const float cf = (GATE && av == b) ? 0.f : s_ctab[(av * (av + 1) / 2 + b) * D + d];
+                const int r0 = kv_row0(av) + 16 * b;
 #pragma unroll
-                for (int nh = 0; nh < 2; ++nh)
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) acc[it][nh][q4] = 0.f;
-            int ia[2], ib[2];
-            bool kk[2];
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                const int blk_id = it == 0 ? warp : 16 + (warp >> 2);
-                kk[it] = blk_id >= NPAIR;
-                const int pr = kk[it] ? blk_id - NPAIR : blk_id;
-                const int aa = pr >= 6 ? 3 : pr >= 3 ? 2 : pr >= 1 ? 1 : 0;
-                ia[it] = aa;
-                ib[it] = pr - aa * (aa + 1) / 2;
+                for (int i = 0; i < 16; ++i)
+                    *reinterpret_cast<float*>(sKV + tc::sw128_offset(r0 + i, d, KV_ROWS)) = tc::to_tf32(kf2[i] * cf);
             }
-            const int kq = warp & 3;
-#pragma unroll 2
-            for (int ks = 0; ks < 16; ++ks) {
-                const int k0 = 8 * ks + t4, k1 = k0 + 4;
+            // the record's (K gamma_C / Gamma)^T: row d, the 16 tokens of sub-chunk b
+            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + 16 * b;
+            const float ec = s_expCE[b * D + d];
 #pragma unroll
-                for (int it = 0; it < 2; ++it) {
-                    if ((it == 0 || (ks >> 2) == kq) && !(GATE && ia[it] == ib[it])) {
-                        const float* Arows = kk[it] ? sKr : sQ;
-                        const int mi = lane >> 3, mr = lane & 7;   // ldmatrix: this lane's matrix and row
-                        uint32_t ra4[4], rb4[4];
-                        // A: rows 16 ia + (0..7 | 8..15), columns 8 ks + (0..3 | 4..7)
-                        ldsm_x4(Arows + (16 * ia[it] + mr + 8 * (mi & 1)) * QS + 8 * ks + 4 * (mi >> 1), ra4);
-                        // B: rows 16 ib + 8 nh + (0..7), columns 8 ks + (0..3 | 4..7), nh = mi >> 1
-                        ldsm_x4(sK + (16 * ib[it] + 8 * (mi >> 1) + mr) * QS + 8 * ks + 4 * (mi & 1), rb4);
-                        const float af[4] = {tc::to_tf32(__uint_as_float(ra4[0])), tc::to_tf32(__uint_as_float(ra4[1])),
-                                             tc::to_tf32(__uint_as_float(ra4[2])), tc::to_tf32(__uint_as_float(ra4[3]))};
-                        const float* ct = s_ctab + (ia[it] * (ia[it] + 1) / 2 + ib[it]) * D;
-                        const float c0f = ct[k0], c1f = ct[k1];
+            for (int t = 0; t < 16; t += 8) {
+                float k8[8];
 #pragma unroll
-                        for (int nh = 0; nh < 2; ++nh) {
-                            const float bfr[2] = {tc::to_tf32(__uint_as_float(rb4[2 * nh]) * c0f),
-                                                  tc::to_tf32(__uint_as_float(rb4[2 * nh + 1]) * c1f)};
-                            tc::mma_m16n8k8_tf32(acc[it][nh], af, bfr);
+                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(kf2[t + u] * ec);
+                st_stream_f8(dst + t, k8);
+            }
+            tc::fence_proxy_async();
+        }
+        __syncthreads();
+        if (tid == 0 && !timed_out) {
+            ++n_mma;
+            tc::fence_after_sync();
+            const uint32_t ab = tc::smem_u32(sQK), bb = tc::smem_u32(sKV);
+#pragma unroll
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_tf32_ss(T0 + TM_G, tc::sw128_desc_k(ab, 2 * C, ks), tc::sw128_desc_k(bb, KV_ROWS, ks),
+                                tc::idesc_tf32(2 * C, KV_ROWS), ks > 0);
+            tc::mma_commit(mbar);
+        }
+        wait(mbar, ph_mma);
+        ph_mma ^= 1u;
+        tc::fence_after_sync();
+        {
+            // row `row` of the result: A_qk row t (row < 64) or A_kk row t (row >= 64), t = row & 63,
+            // of sub-chunk av; its blocks (av, 0..av) are version av's columns.  Quarters 0, 2 of the
+            // lanes (sub-chunks 0, 1) need columns 0..47, quarters 1, 3 (sub-chunks 2, 3) 48..159:
+            // the four warps of a quarter take the 16-column groups in turn.
+            const int t = row & (C - 1), av = t >> 4;
+            const bool kkrow = row >= C;
+            float* Out = kkrow ? sAkk : sAqk;
+            const float bt = kkrow ? s_beta[t] : 0.f;
+            const int g_lo = (quad & 1) ? 3 : 0, g_hi = (quad & 1) ? 10 : 3;
+            for (int g = g_lo + grp; g < g_hi; g += 4) {
+                float v[16];
+                tc::tmem_ld16(T0 + TM_G + lane_base + 16 * g, v);
+                tc::tmem_ld_wait();
+                const int gv = g >= 6 ? 3 : g >= 3 ? 2 : g >= 1 ? 1 : 0;   // version of the group
+                const int j0 = 16 * g - kv_row0(av);                          // key index of column 0
+                // this row's version only; the softplus gate's diagonal comes pair by pair
+                if (gv == av && !(GATE && j0 == 16 * av)) {
+#pragma unroll
+                    for (int u = 0; u < 16; u += 4) {
+                        float4 o4;
+                        float* op = &o4.x;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int J = j0 + u + e;
+                            op[e] = kkrow ? ((J < t) ? v[u + e] * bt : 0.f) : ((J <= t) ? v[u + e] : 0.f);
                         }
+                        *reinterpret_cast<float4*>(Out + t * AS + j0 + u) = o4;
                     }
                 }
+                __syncwarp();   // the next group's TMEM load is warp-collective
             }
-#pragma unroll
-            for (int it = 0; it < 2; ++it) {
-                float* Out = kk[it] ? sAkk : sAqk;
-#pragma unroll
-                for (int nh = 0; nh < 2; ++nh) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int I = 16 * ia[it] + g + 8 * hr;
-                        const int J = 16 * ib[it] + 8 * nh + 2 * t4;
-                        float v0 = acc[it][nh][2 * hr], v1 = acc[it][nh][2 * hr + 1];
-                        if (GATE && ia[it] == ib[it]) continue;   // formed pair by pair
-                        if (it == 1) {   // raw quarter-block partial
-                            *reinterpret_cast<float2*>(part + warp * 256 + (g + 8 * hr) * 16 + 8 * nh + 2 * t4) =
-                                make_float2(v0, v1);
-                            continue;
-                        }
-                        if (!kk[it]) { if (J > I) v0 = 0.f; if (J + 1 > I) v1 = 0.f; }
-                        else {
-                            const float bI = s_beta[I];
-                            v0 = (J >= I) ? 0.f : v0 * bI;
-                            v1 = (J + 1 >= I) ? 0.f : v1 * bI;
-                        }
-                        *reinterpret_cast<float2*>(Out + I * AS + J) = make_float2(v0, v1);
-                    }
-                }
-            }
-            __syncthreads();
             if (GATE) {   // diagonal blocks from the pair-by-pair sums: 2 x 4 blocks of 16 x 16
 #pragma unroll 1
                 for (int x = tid; x < 2 * 4 * 256; x += NTP) {
                     const int kkb = x >> 10, bb = (x >> 8) & 3, i = (x >> 4) & 15, j = x & 15;
                     float val = 0.f;
                     if (j <= i && (j < i || !kkb)) {
-                        const int p = i * (i + 1) / 2 + j, bt = p >> 4, slot = (p & 15) + 16 * kkb;
-                        const float* src = s_diag + ((bb * 9 + bt) * 4) * 32 + slot;
+                        const int p = i * (i + 1) / 2 + j, btc = p >> 4, slot = (p & 15) + 16 * kkb;
+                        const float* src = s_diag + ((bb * 9 + btc) * 4) * 32 + slot;
                         val = (src[0] + src[32]) + (src[64] + src[96]);
                         if (kkb) val *= s_beta[16 * bb + i];
                     }
                     (kkb ? sAkk : sAqk)[(16 * bb + i) * AS + 16 * bb + j] = val;
                 }
-            }
-            if (tid < 256 && (!GATE || (tid >> 6) < 3)) {   // blocks 16..19 = A_kk pairs (3, q)
-                const int q = tid >> 6, e = (tid & 63) * 4;
-                const int I = 48 + (e >> 4), J = 16 * q + (e & 15);
-                const float* pq = part + (4 * q) * 256 + e;   // quarters from warps 4q .. 4q+3
-                const float4 h0 = *reinterpret_cast<const float4*>(pq);
-                const float4 h1 = *reinterpret_cast<const float4*>(pq + 256);
-                const float4 h2 = *reinterpret_cast<const float4*>(pq + 512);
-                const float4 h3 = *reinterpret_cast<const float4*>(pq + 768);
-                const float bI = s_beta[I];
-                float4 o;
-                o.x = (J >= I) ? 0.f : ((h0.x + h1.x) + (h2.x + h3.x)) * bI;
-                o.y = (J + 1 >= I) ? 0.f : ((h0.y + h1.y) + (h2.y + h3.y)) * bI;
-                o.z = (J + 2 >= I) ? 0.f : ((h0.z + h1.z) + (h2.z + h3.z)) * bI;
-                o.w = (J + 3 >= I) ? 0.f : ((h0.w + h1.w) + (h2.w + h3.w)) * bI;
-                *reinterpret_cast<float4*>(sAkk + I * AS + J) = o;
             }
         }
         __syncthreads();
@@ -672,20 +698,17 @@ prep_kernel(kda_prefill_args a, Work w,
         wait(bar_v, ph_v);
         ph_v ^= 1u;
 
-        // ---- 4. B_pre = [V | Gamma K]^T (256 rows), the record's (K gamma_C/Gamma)^T and gamma_C
+        // ---- 4. B_pre = [V | Gamma K]^T (256 rows) and the record's gamma_C
         {
             const int rr = tid & (2 * D - 1), th = tid >> 8;   // B_pre row, half of the tokens
             if (rr < D) {                        // rows 0..127: value columns
                 const int e = rr;
-                const uint8_t* vt = sRawV + (e >> 6) * (C * 128);
 #pragma unroll 4
                 for (int t = 32 * th; t < 32 * th + 32; t += 4) {
                     float4 w4;
                     float* wp = &w4.x;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        wp[u] = (t + u < nc) ? bf16_to_f(*reinterpret_cast<const uint16_t*>(vt + sw128_bf16(t + u, e & 63)))
-                                             : 0.f;
+                    for (int u = 0; u < 4; ++u) wp[u] = (t + u < nc) ? raw_v(t + u, e) : 0.f;
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, 2 * D)) = w4;
                 }
                 if (th == 0) w.gm[rec * GM_FLOATS + e] = s_gam[e];
@@ -697,19 +720,9 @@ prep_kernel(kda_prefill_args a, Work w,
                     float* wp = &w4.x;
                     const float es = s_expS[(t >> 4) * D + d];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(sKr[(t + u) * QS + d] * es);
+                    for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(qk_at(C + t + u, d) * es);
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(D + d, t, 2 * D)) = w4;
                 }
-            }
-            const int d = row;                   // (K gamma_C / Gamma)^T: row d, sub-chunk grp (16 tokens)
-            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + 16 * grp;
-            const float ec = s_expCE[grp * D + d];
-#pragma unroll
-            for (int t = 0; t < 16; t += 8) {
-                float k8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(sK[(16 * grp + t + u) * QS + d] * ec);
-                st_stream_f8(dst + t, k8);
             }
             tc::tmem_st_wait();
             tc::fence_proxy_async();
@@ -720,9 +733,7 @@ prep_kernel(kda_prefill_args a, Work w,
         if (tid == 0 && has_next && !timed_out) {
             ++n_v;
             tc::fence_proxy_async();
-            tc::mbar_arrive_expect_tx(bar_v, BYTES_V);
-            tc::tma_load_2d(sm + OFF_RAWV, &tm_v, nxt.h * D, nxt.t0, bar_v);
-            tc::tma_load_2d(sm + OFF_RAWV + C * 128, &tm_v, nxt.h * D + 64, nxt.t0, bar_v);
+            load_v(nxt);
         }
 
         // ---- 5. MMA 1: D[:, 0:256] = [T beta ; P beta] . [V | Gamma K]
@@ -743,10 +754,7 @@ prep_kernel(kda_prefill_args a, Work w,
         if (tid == 0 && has_next && !timed_out) {
             ++n_in;
             tc::fence_proxy_async();
-            tc::mbar_arrive_expect_tx(bar_in, BYTES_QKZ);
-            tc::tma_load_2d(sm + OFF_RAWQ, &tm_q, nxt.h * D, nxt.t0, bar_in);
-            tc::tma_load_2d(sm + OFF_RAWK, &tm_k, nxt.h * D, nxt.t0, bar_in);
-            tc::tma_load_2d(sm + OFF_RAWZ, &tm_z, nxt.h * D, nxt.t0, bar_in);
+            load_qkz(nxt);
         }
 
         // ---- 6. the record: [U ; U_o] and [-W ; Gamma Q - P Gamma K] (row = lane, 32 columns)
@@ -782,7 +790,7 @@ prep_kernel(kda_prefill_args a, Work w,
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         const int d = 32 * grp + c + j;
-                        const float4 q4 = *reinterpret_cast<const float4*>(sQ + t * QS + d);
+                        const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
                         const float4 e4 = *reinterpret_cast<const float4*>(es + d);
                         o4[j] = tc::to_tf32(q4.x * e4.x - v[j]);
                         o4[j + 1] = tc::to_tf32(q4.y * e4.y - v[j + 1]);
@@ -832,42 +840,38 @@ prep_kernel(kda_prefill_args a, Work w,
 // scan: the state recurrence over one sequence's records
 // ---------------------------------------------------------------------------
 // scan shared-memory / TMEM layout for a cluster of R CTAs per (sequence, head),
-// each owning NE = 128 / R value columns
+// each owning NE = 128 / R value columns.  Ten warps: 0..7 the epilogue
+// (warp w reaches TMEM lanes 32 (w % 4) .. +31 and takes column half w / 4),
+// 8 issues the MMAs and TMEM copies, 9 the TMA loads.
 template <int R>
 struct ScanCfg {
     static constexpr int NE = D / R;
+    static constexpr int WARP_MMA = 8, WARP_LOAD = 9, NTS = 320;
     static constexpr int AW_TILE = 128 * 128 * 4;            // SW128 [128 rows][128 K]
     static constexpr int OFF_AW0 = 0;
     static constexpr int OFF_AW1 = AW_TILE;
     static constexpr int OFF_SOP = 2 * AW_TILE;              // S operand, SW128 [e][d]
     static constexpr int OFF_VOP = OFF_SOP + NE * D * 4;     // V' operand, SW128 [e][t]
     static constexpr int G_TILE = C * NE * 2;                // g_in tile, [C][NE] bf16
-    static constexpr int OFF_G0 = OFF_VOP + NE * C * 4;
-    static constexpr int OFF_G1 = OFF_G0 + G_TILE;
+    static constexpr int OFF_G = OFF_VOP + NE * C * 4;
     static constexpr int KT_BYTES = 128 * C * 4;             // (K gamma_C / Gamma)^T, SW128 [128 rows][C]
-    static constexpr int OFF_RK = OFF_G1 + G_TILE;           // its staging buffer (one chunk)
-    static constexpr int OFF_SMALL = OFF_RK + KT_BYTES;
-    // small region (floats): peers' row sums [2 parity][R source][C], own halves [2][2][C],
-    // RMSNorm weights of this CTA's columns [NE]
+    static constexpr int OFF_K0 = OFF_G + G_TILE;            // MMA 3's A operand, one buffer per chunk parity
+    static constexpr int OFF_K1 = OFF_K0 + KT_BYTES;
+    static constexpr int OFF_SMALL = OFF_K1 + KT_BYTES;
+    // small region (floats): peers' row sums of squares [2 parity][R source][C], this
+    // CTA's half-row sums [2 parity][2 half][C], RMSNorm weights of this CTA's columns [NE]
     static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_NORMW = SM_ROWPART + 4 * C;
     static constexpr int SM_FLOATS = SM_NORMW + NE;
     static constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 256 + 1024;
     static constexpr uint32_t TM_D = 0;                      // 2 x NE cols: [U ; U_o] -> [V' ; O]
-    static constexpr uint32_t TM_A3 = 2 * NE;                // 2 x 64 cols: (K gamma_C / Gamma)^T
-    static constexpr uint32_t TM_DS = TM_A3 + 2 * C;         // NE cols: state increment
+    static constexpr uint32_t TM_DS = 2 * NE;                // NE cols: state increment
     static constexpr uint32_t TM_S = TM_DS + NE;             // NE cols: FP32 state
-    static constexpr uint32_t TM_COLS = (TM_S + NE) <= 256 ? 256 : 512;
-    static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G0 % 1024 == 0 && OFF_RK % 1024 == 0,
+    static constexpr uint32_t TM_COLS = (TM_S + NE) <= 128 ? 128 : 256;
+    static_assert(OFF_SOP % 1024 == 0 && OFF_VOP % 1024 == 0 && OFF_G % 1024 == 0 && OFF_K0 % 1024 == 0,
                   "1024-B aligned operands");
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(TM_S + NE <= TM_COLS, "TMEM budget");
 };
-
-// shared memory -> TMEM: 128 lanes x 256 bits (8 fp32 columns) from the
-// matrix the descriptor describes (the layout an MMA reads as one K = 8 step)
-TC_DEV void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
-}
 
 // 4-byte store into a peer CTA's shared memory that completes 4 transaction bytes
 // on the peer's mbarrier (no fence: the mbarrier phase carries the data)
@@ -876,10 +880,13 @@ TC_DEV void st_async_f32(uint32_t addr, float v, uint32_t mbar_addr) {
                  :: "r"(addr), "r"(__float_as_uint(v)), "r"(mbar_addr) : "memory");
 }
 // arrive on a peer CTA's mbarrier; release at CTA scope orders this CTA's earlier
-// shared-memory reads (gathered by a __syncthreads) before the peer's refill, and
+// shared-memory reads (gathered by a __syncwarp) before the peer's refill, and
 // unlike a cluster-scope release it does not wait for the thread's global traffic
 TC_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+TC_DEV void mbar_arrive_local(uint64_t* mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_u32(mbar)) : "memory");
 }
 TC_DEV bool mbar_try_wait_cluster(uint64_t* mbar, uint32_t parity) {
     uint32_t ok;
@@ -890,6 +897,12 @@ TC_DEV bool mbar_try_wait_cluster(uint64_t* mbar, uint32_t parity) {
         : "=r"(ok) : "r"(tc::smem_u32(mbar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// named barrier among `count` threads.  Every participant syncs (none only arrives):
+// a producer that could pass the barrier without waiting might, when its own waits are
+// skipped after a timeout, run a chunk ahead and add its arrivals to the wrong
+// generation; syncing keeps all participants in lockstep in every case, and costs
+// nothing here since the MMA-issuing warp is always waiting when the others arrive
+TC_DEV void nbar_sync(int id, int count) { asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory"); }
 
 // byte offset of bf16 element (row, col) in a g_in tile of NE columns: the 128-byte
 // rows of NE = 64 come swizzled by TMA, narrower rows are plain
@@ -900,96 +913,102 @@ TC_DEV uint32_t gtile_offset(int row, int col) {
 }
 
 // Per chunk, the recurrence path is MMA 2 -> V' operand -> MMA 3 -> state update.
-// The chunk's output rows take no part in it: the epilogue of chunk j only forms
-// their sums of squares, and o, y of chunk j are written during chunk j+1's
-// MMA 2 from the TMEM buffer that still holds them.  The R CTAs' row sums meet
-// through distributed shared memory behind a split cluster barrier (arrive in
-// chunk j, wait in chunk j+1), so no CTA stalls on its peers.
+// Warp specialisation keeps everything else off it: warp 8 only issues the two
+// MMAs, released by two named barriers (the V' operand of this chunk is written;
+// the state operand of the next chunk is written); warp 9 only issues the TMA
+// loads, each as soon as the buffer it refills is free; the epilogue warps never
+// wait for the other warps except through those barriers.  Both MMAs read their
+// A operand from shared memory, where TMA puts it, so the tensor pipe does
+// nothing but the 24 MMA instructions of the chunk.  The chunk's output rows
+// take no part in the path: the epilogue of chunk j only forms their sums of
+// squares, and o, y of chunk j are written during chunk j+1's MMA 2 from the TMEM
+// buffer that still holds them.  The R CTAs' row sums meet in each peer's shared
+// memory through st.async on mbarriers.
 template <int R>
-__global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(NT, 1)
+__global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(ScanCfg<R>::NTS, 1)
 scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
             const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_kt) {
     using Cfg = ScanCfg<R>;
     constexpr int NE = Cfg::NE;
-    constexpr int HW = NE / 2;           // value columns per thread
+    constexpr int HW = NE / 2;           // value columns per epilogue thread
+    constexpr int NB_V = 1, NB_S = 2, NB_O = 3;   // named barriers
+    constexpr int NV = 5 * 32;           // V' warps (0, 1, 4, 5) + the MMA warp
+    constexpr int NS = 9 * 32;           // epilogue warps + the MMA warp
+    constexpr int NO = 4 * 32;           // output-row warps (2, 3, 6, 7)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sSop = sm + Cfg::OFF_SOP;
     uint8_t* sVop = sm + Cfg::OFF_VOP;
     float* fs = reinterpret_cast<float*>(sm + Cfg::OFF_SMALL);
     float* s_rowsq = fs + Cfg::SM_ROWSQ;      // [2][R][C] peers' row sums, by parity and source
-    float* s_rowpart = fs + Cfg::SM_ROWPART;  // [2][2][C] this CTA's, by parity and column half
+    float* s_rowpart = fs + Cfg::SM_ROWPART;  // [2][2][C] this CTA's, by parity and half
     float* s_normw = fs + Cfg::SM_NORMW;      // [NE] RMSNorm weights (ones without norm_w)
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + Cfg::SM_FLOATS);
-    uint64_t* bar_aw = mbar + 1;         // [2]
-    uint64_t* bar_g = mbar + 3;          // [2]
-    uint64_t* bar_full = mbar + 5;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
-    uint64_t* bar_free = mbar + 7;       // [2][R] peer p has read this CTA's row sums of chunk j
-    uint64_t* bar_rk = mbar + 7 + 2 * R; // staged (K gamma_C / Gamma)^T landed
-    uint64_t* bar_ck = bar_rk + 1;       // its copy into TMEM is done (the staging buffer is free)
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_rk + 2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(fs + Cfg::SM_FLOATS);
+    uint64_t* bar_m2 = bars;             // MMA 2 of chunk j done (phase j)
+    uint64_t* bar_m3 = bars + 1;         // MMA 3 of chunk j done (phase j)
+    uint64_t* bar_aw = bars + 2;         // [2] A tile of chunk j landed in buffer j & 1
+    uint64_t* bar_g = bars + 4;          // g_in tile of chunk j landed (phase j)
+    uint64_t* bar_gfree = bars + 5;      // the output warps have read the g_in tile of chunk j
+    uint64_t* bar_full = bars + 6;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
+    uint64_t* bar_free = bars + 8;       // [2][R] peer p has read this CTA's sums of chunk j
+    uint64_t* bar_k = bars + 8 + 2 * R;  // [2] (K gamma_C / Gamma)^T of chunk j landed in buffer j & 1
+    uint64_t* bar_awfree = bar_k + 2;    // [2] MMA 2 has read A-tile buffer b (one phase per use)
+    uint64_t* bar_kfree = bar_awfree + 2;   // [2] MMA 3 has read K buffer b (one phase per use)
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_kfree + 2);
 
     const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
     const int n = blockIdx.z;
     const int H = a.H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, hf = warp >> 2;
+    const bool epi = warp < 8;
+    const int quad = warp & 3, hf = (warp >> 2) & 1;
     const int row = quad * 32 + lane;
     const int c_lo = hf * HW;
+    const bool vrow = epi && quad < 2;   // V' rows (tokens) 0..63; else output rows 64..127
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const int t_begin = a.cu_seqlens[n], t_end = a.cu_seqlens[n + 1];
     const int g0 = w.chunk_base[n];
     const int nch = w.chunk_base[n + 1] - g0;
     const bool gate = a.g_in != nullptr;
+    const int din = a.dk;            // 128, or a float32 operator's d <= 64 (the rest is zero padding)
     auto rec_of = [&](int j) { return (long)(g0 + j) * H + h; };
     auto aw_buf = [&](int b) { return sm + (b ? Cfg::OFF_AW1 : Cfg::OFF_AW0); };
-    auto g_buf = [&](int b) { return sm + (b ? Cfg::OFF_G1 : Cfg::OFF_G0); };
+    auto k_buf = [&](int b) { return sm + (b ? Cfg::OFF_K1 : Cfg::OFF_K0); };
+    uint8_t* sG = sm + Cfg::OFF_G;
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
     if (tid < NE) s_normw[tid] = a.norm_w ? a.norm_w[NE * r + tid] : 1.f;
-    // thread 0 issues every copy and MMA and arms the row-sum barriers; it counts
-    // the phases it issued on each mbarrier, for the give-up path at the end
-    uint32_t n_aw[2] = {0, 0}, n_g[2] = {0, 0}, n_full[2] = {0, 0}, n_rk = 0, n_ck = 0, n_mma = 0;
     if (tid == 0) {
-        tc::mbar_init(mbar, 1);
+        tc::mbar_init(bar_m2, 1);
+        tc::mbar_init(bar_m3, 1);
+        tc::mbar_init(bar_g, 1);
+        tc::mbar_init(bar_gfree, 4);                  // one arrival per output warp
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(bar_aw + b, 1);
-            tc::mbar_init(bar_g + b, 1);
             tc::mbar_init(bar_full + b, 1);
-            for (int p = 0; p < R; ++p) tc::mbar_init(bar_free + b * R + p, 1);
+            for (int p = 0; p < R; ++p) tc::mbar_init(bar_free + b * R + p, 4);   // peer p's output warps
+            tc::mbar_init(bar_k + b, 1);
+            tc::mbar_init(bar_awfree + b, 1);
+            tc::mbar_init(bar_kfree + b, 1);
         }
-        tc::mbar_init(bar_rk, 1);
-        tc::mbar_init(bar_ck, 1);
         tc::mbar_fence_init();
-        tc::tma_prefetch_desc(&tm_aw);
-        tc::tma_prefetch_desc(&tm_kt);
-        if (gate) tc::tma_prefetch_desc(&tm_g);
-        for (int j = 0; j < 2 && j < nch; ++j) {
-            ++n_aw[j];
-            if (gate) ++n_g[j];
-            tc::mbar_arrive_expect_tx(bar_aw + j, Cfg::AW_TILE);
-            for (int s = 0; s < 4; ++s)
-                tc::tma_load_2d(aw_buf(j) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + j);
-            if (gate) {
-                tc::mbar_arrive_expect_tx(bar_g + j, Cfg::G_TILE);
-                tc::tma_load_2d(g_buf(j), &tm_g, h * D + NE * r, t_begin + C * j, bar_g + j);
-            }
-        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t T0 = *tbase_ptr;
-    uint32_t ph_mma = 0;
+    if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
+
     // A wait on a local copy or MMA that gives up records it in timed_out: this
-    // thread then skips every later such wait, and thread 0 issues no further
-    // copy or MMA, so the kernel runs to its end (its results are invalid) and
-    // drains what was issued.  The row-sum exchange with the peer CTAs keeps
-    // running (its data are then meaningless, its protocol intact) so that no
-    // peer is left waiting and no row sum lands after a CTA has exited; a wait
-    // of that exchange that gives up (a peer that stopped) sets xdead, after
-    // which this thread stops exchanging.
+    // thread then skips every later such wait, and the issuing lanes (warp 8 and
+    // warp 9, lane 0) issue no further copy or MMA, so the kernel runs to its end
+    // (its results are invalid) and drains what was issued.  The named barriers
+    // and the row-sum exchange with the peer CTAs keep running (their data are
+    // then meaningless, their protocol intact), so that no warp or peer is left
+    // waiting and nothing lands after a CTA has exited; a wait of the exchange
+    // that gives up (a peer that stopped) sets xdead, after which this thread
+    // stops exchanging.
     bool timed_out = false, xdead = false;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         if (!timed_out && !tc::mbar_wait_bounded(bar, parity, w.wait_limit)) timed_out = true;
@@ -998,187 +1017,230 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         for (uint32_t i = 0; !xdead && !mbar_try_wait_cluster(bar, parity); )
             if (++i == tc::WAIT_POLLS) xdead = true;
     };
-    auto mma_wait = [&]() {
-        wait(mbar, ph_mma);
-        ph_mma ^= 1u;
-        tc::fence_after_sync();
-    };
+    // phases each issuing lane armed or issued on each mbarrier, for the drain
+    uint32_t n_aw[2] = {0, 0}, n_k[2] = {0, 0}, n_full[2] = {0, 0}, n_g = 0;
+    uint32_t n_m2 = 0, n_m3 = 0, n_awf[2] = {0, 0}, n_kf[2] = {0, 0};
 
-    // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
-    // CTA's columns, and gamma_C[row]; (K gamma_C / Gamma)^T, the same for the
-    // four CTAs, goes by TMA into a staging buffer and from there by tcgen05.cp
-    // into TMEM, both issued by thread 0
-    float pu[HW], pg = 0.f;
-    auto load_rec = [&](int j) {
-        const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
-        if (!w.zero_v) {
-#pragma unroll
-            for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
-        }
-        pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
-    };
-    auto store_rec = [&](int b) {
-        if (!w.zero_v) {
-#pragma unroll
-            for (int i = 0; i < HW; i += 16)
-                tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
-        }
-    };
-    uint8_t* sRk = sm + Cfg::OFF_RK;
-    uint32_t ph_rk = 0, ph_ck = 0;   // thread 0's phases
-    auto tma_k = [&](int j) {
-        ++n_rk;
-        tc::mbar_arrive_expect_tx(bar_rk, Cfg::KT_BYTES);
-#pragma unroll
-        for (int s = 0; s < C / 32; ++s)
-            tc::tma_load_2d(sRk + s * (128 * 32 * 4), &tm_kt, 32 * s, (int)(rec_of(j) * 128), bar_rk);
-    };
-    auto cp_k = [&](int b) {   // staged (K gamma_C / Gamma)^T -> TMEM buffer b
-        wait(bar_rk, ph_rk);
-        ph_rk ^= 1u;
-        if (timed_out) return;
-        tc::fence_after_sync();
-        const uint32_t sk = tc::smem_u32(sRk);
-#pragma unroll
-        for (int kc = 0; kc < C / 8; ++kc)
-            tmem_cp_128x256b(T0 + Cfg::TM_A3 + C * b + 8 * kc, tc::sw128_desc_k(sk, 128, kc));
-    };
-    // o and y of chunk jo from its TMEM buffer (output-row threads, row >= C)
-    auto emit_outputs = [&](int jo) {
-        const int bo = jo & 1;
-        const int t = row - C;
-        const int c0o = t_begin + C * jo;
-        const int nco = min(C, t_end - c0o);
-        float o[HW];
-#pragma unroll
-        for (int c = 0; c < HW; c += 16) tc::tmem_ld16(T0 + Cfg::TM_D + NE * bo + lane_base + c_lo + c, o + c);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < HW; ++c) o[c] *= a.scale;
-        if (t < nco && a.o) {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
-#pragma unroll
-            for (int c = 0; c < HW; c += 8) store8_bf16(dst + c, o + c);
-        }
-        if (gate) {
-            wait(bar_g + bo, (jo >> 1) & 1);
-            wait_cl(bar_full + bo, (jo >> 1) & 1);
-            if (t < nco) {
-                const uint8_t* sG = g_buf(bo);
-                float tot = s_rowpart[(bo * 2) * C + t] + s_rowpart[(bo * 2 + 1) * C + t];
-#pragma unroll
-                for (int p = 0; p < R; ++p)
-                    if (p != r) tot += s_rowsq[(bo * R + p) * C + t];
-                const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
-                uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
-#pragma unroll
-                for (int c = 0; c < HW; c += 8) {
-                    const uint4 g8 = *reinterpret_cast<const uint4*>(sG + gtile_offset<NE>(t, c_lo + c));
-                    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
-                    const float4 wa = reinterpret_cast<const float4*>(s_normw + c_lo + c)[0];
-                    const float4 wb = reinterpret_cast<const float4*>(s_normw + c_lo + c)[1];
-                    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-                    float yv[8];
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
-                        yv[jj] = __fdividef(o[c + jj] * wv[jj] * rr, 1.0f + __expf(-gv));
-                    }
-                    store8_bf16(yp + c, yv);
-                }
-            }
-        }
-    };
-
-    // ---- initial state -> TMEM master copy and the tf32 operand copy
-    if (tid == 0 && nch > 0) tma_k(0);   // before any wait: thread 0 has not timed out
-    float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
-    {
-        const int d = row;
-        const size_t sb = (((size_t)n * H + h) * D + d) * D + NE * r;
-        float v[16];
-#pragma unroll
-        for (int c = c_lo; c < c_lo + HW; c += 16) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj) v[jj] = a.S0 ? a.S0[sb + c + jj] : 0.f;
-            tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, v);
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-                *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(v[jj]);
-        }
-        if (nch > 0) { load_rec(0); store_rec(0); gm_next = pg; }
-        if (nch > 1) load_rec(1);
-        tc::tmem_st_wait();
-        tc::fence_proxy_async();
-    }
-    if (tid == 0 && nch > 0) {
-        cp_k(0);
-        if (!timed_out) { ++n_mma; tc::mma_commit(mbar); }
-    }
-    if (nch > 0) mma_wait();   // every thread: keeps the MMA phase in step
-    if (tid == 0 && nch > 1 && !timed_out) tma_k(1);
-    tc::fence_before_sync();
-    __syncthreads();
-    if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
-
-#pragma unroll 1
-    for (int j = 0; j < nch; ++j) {
-        const int b = j & 1;
-        const int c0 = t_begin + C * j;
-        const int nc = min(C, t_end - c0);
-        const float gm = gm_next;
-
-        // ---- MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S  (U = 0 under zero_v:
-        //      the first step then ignores the accumulator)
-        if (tid == 0) {
-            wait(bar_aw + b, (j >> 1) & 1);
-            if (!timed_out) {
-                tc::fence_after_sync();
-                const uint32_t ab = tc::smem_u32(aw_buf(b));
-                const uint32_t sb = tc::smem_u32(sSop);
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks),
-                                    tc::sw128_desc_k(sb, NE, ks), tc::idesc_tf32(128, NE),
-                                    (ks > 0 || !w.zero_v) ? 1u : 0u);
-                ++n_mma;
-                tc::mma_commit(mbar);
-            }
-            // the peers' row sums of this chunk (phase j - 2 of this barrier completed
-            // before the previous chunk's closing __syncthreads; a peer that stopped
-            // leaves it open, and then the barrier is not armed again)
-            if (gate && !xdead) {
-                if (j >= 2 && !tc::mbar_try_wait(bar_full + b, ((j - 2) >> 1) & 1)) xdead = true;
-                else { ++n_full[b]; tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4); }
-            }
-            // the next chunk's (K gamma_C / Gamma)^T into TMEM buffer b ^ 1 (its last
-            // reader, MMA 3 of chunk j - 1, has completed)
-            if (j + 1 < nch && !timed_out) {
-                cp_k(b ^ 1);
-                if (!timed_out) { ++n_ck; tc::mma_commit(bar_ck); }
-            }
-        }
-        // while it runs: outputs of the previous chunk (their buffer is refilled next),
-        // the next record into the other TMEM buffers, the one after it into registers
-        if (j > 0 && row >= C && (a.o || gate)) emit_outputs(j - 1);
-        if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
-        if (j + 2 < nch) load_rec(j + 2);
-        tc::tmem_st_wait();
-        mma_wait();
-        if (tid == 0 && !timed_out) {
-            if (j + 2 < nch) {   // the A tile of this chunk is consumed
+    if (warp == Cfg::WARP_LOAD) {
+        // ------------------------------------------------------------------ TMA loads
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tm_aw);
+            tc::tma_prefetch_desc(&tm_kt);
+            if (gate) tc::tma_prefetch_desc(&tm_g);
+            auto load_aw = [&](int j) {
+                const int b = j & 1;
                 ++n_aw[b];
                 tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
                 for (int s = 0; s < 4; ++s)
-                    tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j + 2) * 128), bar_aw + b);
+                    tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + b);
+            };
+            auto load_g = [&](int j) {
+                ++n_g;
+                tc::mbar_arrive_expect_tx(bar_g, Cfg::G_TILE);
+                tc::tma_load_2d(sG, &tm_g, h * D + NE * r, t_begin + C * j, bar_g);
+            };
+            auto load_k = [&](int j) {   // both 32-token halves of chunk j's K^T
+                const int b = j & 1;
+                ++n_k[b];
+                tc::mbar_arrive_expect_tx(bar_k + b, Cfg::KT_BYTES);
+                for (int hh = 0; hh < 2; ++hh)
+                    tc::tma_load_2d(k_buf(b) + hh * (Cfg::KT_BYTES / 2), &tm_kt, 32 * hh, (int)(rec_of(j) * 128),
+                                    bar_k + b);
+            };
+            for (int j = 0; j < 2 && j < nch; ++j) { load_aw(j); load_k(j); }
+            if (gate && nch > 0) load_g(0);
+            for (int j = 0; j < nch && !timed_out; ++j) {
+                // buffers j & 1 of chunk j + 2 once MMA 2 / MMA 3 of chunk j have read them
+                // (barriers of those buffers' own: their next phases need these very loads,
+                // so they cannot run a phase ahead of the waits)
+                if (j + 2 < nch) { wait(bar_awfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_aw(j + 2); }
+                if (j + 2 < nch) { wait(bar_kfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_k(j + 2); }
+                // the g_in tile of chunk j + 1 once the outputs of chunk j are written
+                if (gate && j + 1 < nch) { wait(bar_gfree, j & 1); if (!timed_out) load_g(j + 1); }
             }
         }
+        __syncwarp();
+    } else if (warp == Cfg::WARP_MMA) {
+        // ------------------------------------------------------------------ MMA issue
+#pragma unroll 1
+        for (int j = 0; j < nch; ++j) {
+            const int b = j & 1;
+            nbar_sync(NB_S, NS);   // the state operand of chunk j is written
+            if (lane == 0) {
+                wait(bar_aw + b, (j >> 1) & 1);
+                if (!timed_out) {   // MMA 2: [V' ; O] = [U ; U_o] + [-W ; Gamma Q - P Gamma K] . S
+                    tc::fence_after_sync();
+                    const uint32_t ab = tc::smem_u32(aw_buf(b));
+                    const uint32_t sb = tc::smem_u32(sSop);
+#pragma unroll
+                    for (int ks = 0; ks < D / 8; ++ks)
+                        tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks),
+                                        tc::sw128_desc_k(sb, NE, ks), tc::idesc_tf32(128, NE),
+                                        (ks > 0 || !w.zero_v) ? 1u : 0u);
+                    ++n_m2;
+                    tc::mma_commit(bar_m2);
+                    ++n_awf[b];
+                    tc::mma_commit(bar_awfree + b);
+                }
+                wait(bar_k + b, (j >> 1) & 1);   // lands long before: loaded two chunks ahead
+            }
+            __syncwarp();
+            nbar_sync(NB_V, NV);   // the V' operand of chunk j is written
+            if (lane == 0 && !timed_out) {   // MMA 3: dS = (K gamma_C / Gamma)^T . V'
+                tc::fence_after_sync();
+                const uint32_t kb = tc::smem_u32(k_buf(b));
+                const uint32_t vb = tc::smem_u32(sVop);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_tf32_ss(T0 + Cfg::TM_DS, tc::sw128_desc_k(kb, 128, ks), tc::sw128_desc_k(vb, NE, ks),
+                                    tc::idesc_tf32(128, NE), ks > 0);
+                ++n_m3;
+                tc::mma_commit(bar_m3);
+                ++n_kf[b];
+                tc::mma_commit(bar_kfree + b);
+            }
+            __syncwarp();
+        }
+        nbar_sync(NB_S, NS);       // the epilogue's last arrival
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
+        // CTA's columns, and gamma_C[row]
+        float pu[HW], pg = 0.f;
+        auto load_rec = [&](int j) {
+            const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
+            if (!w.zero_v) {
+#pragma unroll
+                for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
+            }
+            pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
+        };
+        auto store_rec = [&](int b) {
+            if (!w.zero_v) {
+#pragma unroll
+                for (int i = 0; i < HW; i += 16)
+                    tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
+            }
+        };
+        // o and y of chunk jo from its TMEM buffer (output-row threads)
+        auto emit_outputs = [&](int jo) {
+            const int bo = jo & 1;
+            const int t = row - C;
+            const int c0o = t_begin + C * jo;
+            const int nco = min(C, t_end - c0o);
+            float o[HW];
+#pragma unroll
+            for (int c = 0; c < HW; c += 16) tc::tmem_ld16(T0 + Cfg::TM_D + NE * bo + lane_base + c_lo + c, o + c);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < HW; ++c) o[c] *= a.scale;
+            if (t < nco && a.o) {
+                if (din == D) {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+                    for (int c = 0; c < HW; c += 8) store8_bf16(dst + c, o + c);
+                } else {       // float32 o of d_v = din < 128 columns
+                    float* dst = reinterpret_cast<float*>(a.o) + ((size_t)(c0o + t) * H + h) * din;
+#pragma unroll
+                    for (int c = 0; c < HW; ++c)
+                        if (NE * r + c_lo + c < din) dst[NE * r + c_lo + c] = o[c];
+                }
+            }
+            if (gate) {
+                wait(bar_g, jo & 1);
+                wait_cl(bar_full + bo, (jo >> 1) & 1);
+                if (t < nco) {
+                    float tot = s_rowpart[(bo * 2) * C + t] + s_rowpart[(bo * 2 + 1) * C + t];
+#pragma unroll
+                    for (int p = 0; p < R; ++p)
+                        if (p != r) tot += s_rowsq[(bo * R + p) * C + t];
+                    const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
+                    uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
+#pragma unroll
+                    for (int c = 0; c < HW; c += 8) {
+                        const uint4 g8 = *reinterpret_cast<const uint4*>(sG + gtile_offset<NE>(t, c_lo + c));
+                        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                        const float4 wa = reinterpret_cast<const float4*>(s_normw + c_lo + c)[0];
+                        const float4 wb = reinterpret_cast<const float4*>(s_normw + c_lo + c)[1];
+                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                        float yv[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
+                            yv[jj] = __fdividef(o[c + jj] * wv[jj] * rr, 1.0f + __expf(-gv));
+                        }
+                        store8_bf16(yp + c, yv);
+                    }
+                }
+            }
+        };
 
-        // ---- V' -> operand (smem); output rows: sums of squares for the gate
+        // ---- initial state -> TMEM master copy and the tf32 operand copy
+        float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
         {
+            const int d = row;
+            const size_t sb = (((size_t)n * H + h) * din + d) * din + NE * r;
             float v[16];
-            if (row < C) {
+#pragma unroll
+            for (int c = c_lo; c < c_lo + HW; c += 16) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    v[jj] = (a.S0 && d < din && NE * r + c + jj < din) ? a.S0[sb + c + jj] : 0.f;
+                tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, v);
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj)
+                    *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(v[jj]);
+            }
+            if (nch > 0) { load_rec(0); store_rec(0); gm_next = pg; }
+            if (nch > 1) load_rec(1);
+            tc::tmem_st_wait();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+        }
+        nbar_sync(NB_S, NS);
+
+#pragma unroll 1
+        for (int j = 0; j < nch; ++j) {
+            const int b = j & 1;
+            const int c0 = t_begin + C * j;
+            const int nc = min(C, t_end - c0);
+            const float gm = gm_next;
+
+            // ---- while MMA 2 runs: outputs of the previous chunk (their buffer is
+            //      refilled next), the next record into the other TMEM buffer, the one
+            //      after it into registers
+            if (!vrow) {
+                if (j > 0 && (a.o || gate)) {
+                    emit_outputs(j - 1);
+                    if (gate) {
+                        // the g_in tile and the peers' sums of chunk j - 1 are read
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive_local(bar_gfree);
+#pragma unroll
+                            for (int p = 1; p < R; ++p)
+                                mbar_arrive_remote(cluster_map(bar_free + (b ^ 1) * R + r, (r + p) % R));
+                        }
+                    }
+                }
+                // arm this chunk's exchange barrier (its phase for chunk j - 2 completed:
+                // this thread waited for it in emit_outputs; a peer that stopped leaves
+                // it open, and then it is not armed again)
+                if (gate && warp == 2 && lane == 0 && !xdead) {
+                    if (j >= 2 && !tc::mbar_try_wait(bar_full + b, ((j - 2) >> 1) & 1)) xdead = true;
+                    else { ++n_full[b]; tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4); }
+                }
+            }
+            if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
+            if (j + 2 < nch) load_rec(j + 2);
+            tc::tmem_st_wait();
+            wait(bar_m2, j & 1);
+            tc::fence_after_sync();
+
+            // ---- V' -> MMA 3 operand (smem); output rows: half-row sums of squares
+            if (vrow) {
                 const int t = row;
+                float v[16];
 #pragma unroll
                 for (int c = c_lo; c < c_lo + HW; c += 16) {
                     tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
@@ -1187,9 +1249,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     for (int jj = 0; jj < 16; ++jj)
                         *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + jj, t, NE)) = tc::to_tf32(v[jj]);
                 }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                nbar_sync(NB_V, NV);
             } else if (gate) {
                 const int t = row - C;
-                float ss = 0.f;
+                float v[16], ss = 0.f;
 #pragma unroll
                 for (int c = c_lo; c < c_lo + HW; c += 16) {
                     tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
@@ -1197,129 +1262,112 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) ss = fmaf(v[jj], v[jj], ss);
                 }
-                s_rowpart[(b * 2 + hf) * C + t] = ss * a.scale * a.scale;
+                ss *= a.scale * a.scale;
+                s_rowpart[(b * 2 + hf) * C + t] = ss;
+                nbar_sync(NB_O, NO);   // both halves of this chunk's sums are in s_rowpart
+                // the row's sum over this CTA's columns into every peer's s_rowsq[b] (by the
+                // first half's thread), once every peer has read what this CTA wrote there
+                // for chunk j - 2 (one barrier per peer: a peer's signals reach it in
+                // order, different peers' need not)
+                if (hf == 0) {
+                    if (j >= 2) {
+#pragma unroll
+                        for (int p = 1; p < R; ++p) wait_cl(bar_free + b * R + (r + p) % R, ((j - 2) >> 1) & 1);
+                    }
+                    const float own = ss + s_rowpart[(b * 2 + 1) * C + t];
+                    if (!xdead) {
+#pragma unroll
+                        for (int p = 1; p < R; ++p)
+                            st_async_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own,
+                                         cluster_map(bar_full + b, (r + p) % R));
+                    }
+                }
             }
-            tc::fence_proxy_async();
-            tc::fence_before_sync();
-        }
-        __syncthreads();
 
-        // ---- MMA 3: dS = (K gamma_C / Gamma)^T . V'
-        if (tid == 0 && !timed_out) {
+            // ---- S = Diag(gamma_C) S + dS (FP32 in TMEM), refresh the tf32 operand copy;
+            //      a chunk that closes a prefix-cache interval also writes S out
+            wait(bar_m3, j & 1);
             tc::fence_after_sync();
-            const uint32_t vb = tc::smem_u32(sVop);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(T0 + Cfg::TM_DS, T0 + Cfg::TM_A3 + C * b + 8 * ks, tc::sw128_desc_k(vb, NE, ks),
-                                tc::idesc_tf32(128, NE), ks > 0);
-            ++n_mma;
-            tc::mma_commit(mbar);
-            if (j + 1 < nch) {   // the staging buffer is free once the K copy is done (waited
-                                 // here, after the chunk's first barrier, off the path into it)
-                wait(bar_ck, ph_ck);
-                ph_ck ^= 1u;
-                if (j + 2 < nch && !timed_out) tma_k(j + 2);
-            }
-            // the g_in tile of chunk j-1 is consumed (its outputs were emitted above;
-            // the output-row threads waited for it, so its phase is complete unless
-            // one of their waits gave up -- then nothing more is issued)
-            if (gate && j >= 1 && j + 1 < nch && !timed_out &&
-                !tc::mbar_try_wait(bar_g + (b ^ 1), ((j - 1) >> 1) & 1))
-                timed_out = true;
-            if (gate && j >= 1 && j + 1 < nch && !timed_out) {
-                ++n_g[b ^ 1];
-                tc::mbar_arrive_expect_tx(bar_g + (b ^ 1), Cfg::G_TILE);
-                tc::tma_load_2d(g_buf(b ^ 1), &tm_g, h * D + NE * r, t_begin + C * (j + 1), bar_g + (b ^ 1));
-            }
-        }
-        if (gate) {
-            // this chunk's row sums into every peer's s_rowsq[b], once every peer has
-            // read what this CTA wrote there for chunk j - 2 (one barrier per peer: a
-            // peer's signals reach it in order, different peers' need not)
-            if (row < C && hf == 1) {   // warps 4, 5: no MMA issue on their path
-                const int t = row;
-                if (j >= 2) {
-#pragma unroll
-                    for (int p = 1; p < R; ++p) wait_cl(bar_free + b * R + (r + p) % R, ((j - 2) >> 1) & 1);
+            {
+                const int d = row;
+                float* snap = nullptr;
+                if (a.S_snap && (c0 + nc - t_begin) % a.snap_interval == 0) {
+                    const long srow = snapshot_row_base(a.cu_seqlens, n, a.snap_interval) +
+                                      (c0 + nc - t_begin) / a.snap_interval - 1;
+                    snap = a.S_snap + ((srow * H + h) * din + d) * din + NE * r;
                 }
-                const float own = s_rowpart[(b * 2) * C + t] + s_rowpart[(b * 2 + 1) * C + t];
-                if (!xdead) {
+                float dv[16], sv[16];
 #pragma unroll
-                    for (int p = 1; p < R; ++p)
-                        st_async_f32(cluster_map(s_rowsq + (b * R + r) * C + t, (r + p) % R), own,
-                                     cluster_map(bar_full + b, (r + p) % R));
+                for (int c = c_lo; c < c_lo + HW; c += 16) {
+                    tc::tmem_ld16(T0 + Cfg::TM_DS + lane_base + c, dv);
+                    tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, sv);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
+                    tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, sv);
+                    if (snap && din == D) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; jj += 4)
+                            *reinterpret_cast<float4*>(snap + c + jj) = make_float4(sv[jj], sv[jj + 1], sv[jj + 2], sv[jj + 3]);
+                    } else if (snap && d < din) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (NE * r + c + jj < din) snap[c + jj] = sv[jj];
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(sv[jj]);
                 }
+                tc::tmem_st_wait();
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
             }
-            // the outputs of chunk j - 1 (read before the __syncthreads above) are out:
-            // each peer may overwrite s_rowsq[(j - 1) & 1] with its sums of chunk j + 1
-            if (tid == 32 && j >= 1 && j + 1 < nch) {
-#pragma unroll
-                for (int p = 1; p < R; ++p) mbar_arrive_remote(cluster_map(bar_free + (b ^ 1) * R + r, (r + p) % R));
-            }
+            nbar_sync(NB_S, NS);
         }
+        // outputs of the last chunk
+        if (nch > 0 && !vrow && (a.o || gate)) emit_outputs(nch - 1);
 
-        // ---- S = Diag(gamma_C) S + dS (FP32 in TMEM), refresh the tf32 operand copy;
-        //      a chunk that closes a prefix-cache interval also writes S out
-        mma_wait();
-        {
+        // ---- final state
+        if (a.S_T) {
             const int d = row;
-            float* snap = nullptr;
-            if (a.S_snap && (c0 + nc - t_begin) % a.snap_interval == 0) {
-                const long srow = snapshot_row_base(a.cu_seqlens, n, a.snap_interval) +
-                                  (c0 + nc - t_begin) / a.snap_interval - 1;
-                snap = a.S_snap + ((srow * H + h) * D + d) * D + NE * r;
-            }
-            float dv[16], sv[16];
+            float* dst = a.S_T + (((size_t)n * H + h) * din + d) * din + NE * r;
+            float v[16];
 #pragma unroll
             for (int c = c_lo; c < c_lo + HW; c += 16) {
-                tc::tmem_ld16(T0 + Cfg::TM_DS + lane_base + c, dv);
-                tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, sv);
+                tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, v);
                 tc::tmem_ld_wait();
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
-                tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, sv);
-                if (snap) {
+                if (din == D) {
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4)
-                        *reinterpret_cast<float4*>(snap + c + jj) = make_float4(sv[jj], sv[jj + 1], sv[jj + 2], sv[jj + 3]);
+                        *reinterpret_cast<float4*>(dst + c + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+                } else if (d < din) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        if (NE * r + c + jj < din) dst[c + jj] = v[jj];
                 }
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(sv[jj]);
             }
-            tc::tmem_st_wait();
-            tc::fence_proxy_async();
-            tc::fence_before_sync();
         }
-        __syncthreads();
     }
-    // outputs of the last chunk
-    if (nch > 0 && row >= C && (a.o || gate)) emit_outputs(nch - 1);
 
-    // ---- final state
-    if (a.S_T) {
-        const int d = row;
-        float* dst = a.S_T + (((size_t)n * H + h) * D + d) * D + NE * r;
-        float v[16];
+    // give-up path: each issuing lane waits for the copies and tensor-core work it
+    // issued, and the lane that armed the exchange barriers for the peers' sums,
+    // before any of this CTA's shared memory or TMEM is released
+    if (__syncthreads_or(timed_out || xdead)) {
+        bool drained = true;
+        if (warp == Cfg::WARP_MMA && lane == 0)
+            drained = tc::drain_phase(bar_m2, n_m2) & tc::drain_phase(bar_m3, n_m3) &
+                      tc::drain_phase(bar_awfree, n_awf[0]) & tc::drain_phase(bar_awfree + 1, n_awf[1]) &
+                      tc::drain_phase(bar_kfree, n_kf[0]) & tc::drain_phase(bar_kfree + 1, n_kf[1]);
+        if (warp == Cfg::WARP_LOAD && lane == 0) {
+            drained = tc::drain_phase(bar_g, n_g);
 #pragma unroll
-        for (int c = c_lo; c < c_lo + HW; c += 16) {
-            tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < 16; jj += 4)
-                *reinterpret_cast<float4*>(dst + c + jj) = make_float4(v[jj], v[jj + 1], v[jj + 2], v[jj + 3]);
+            for (int b = 0; b < 2; ++b)
+                drained = drained & tc::drain_phase(bar_aw + b, n_aw[b]) & tc::drain_phase(bar_k + b, n_k[b]);
         }
-    }
-    // give-up path: wait for the copies and tensor-core work thread 0 issued and
-    // for the peers' row sums of the phases it armed, before any of this CTA's
-    // shared memory or TMEM is released
-    if (__syncthreads_or(timed_out || xdead) && tid == 0) {
-        bool drained = tc::drain_phase(mbar, n_mma) & tc::drain_phase(bar_ck, n_ck) & tc::drain_phase(bar_rk, n_rk);
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-            drained = drained & tc::drain_phase(bar_aw + b, n_aw[b]) & tc::drain_phase(bar_g + b, n_g[b]) &
-                      tc::drain_phase(bar_full + b, n_full[b]);
-        atomicOr(w.err, drained ? tc::ERR_WAIT : tc::ERR_WAIT | tc::ERR_DRAIN);
+        if (warp == 2 && lane == 0)
+            drained = tc::drain_phase(bar_full, n_full[0]) & tc::drain_phase(bar_full + 1, n_full[1]);
+        if ((warp == Cfg::WARP_MMA || warp == Cfg::WARP_LOAD || warp == 2) && lane == 0)
+            atomicOr(w.err, drained ? tc::ERR_WAIT : tc::ERR_WAIT | tc::ERR_DRAIN);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -1368,16 +1416,25 @@ static int sm_count() {
 
 size_t prefill_split_workspace_size(const kda_prefill_args& a) { return spl::layout(a).total; }
 
+// bf16 q/k/v with d = 128, or float32 q/k/v with d = 32 or 64 (zero-padded to 128)
+bool prefill_split_supported(const kda_prefill_args& a) {
+    if (a.dk != a.dv) return false;
+    if (a.qkv_dtype == KDA_BF16) return a.dk == spl::D;
+    return a.qkv_dtype == KDA_F32 && (a.dk == 32 || a.dk == spl::prep::DIN_MAX);
+}
+
 // parts: bit 0 = plan + prep (the records), bit 1 = scan; scan_flags: KDA_SCAN_*
 cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int scan_flags, cudaStream_t s) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(spl::prep_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        spl::prep::SMEM_BYTES);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(spl::prep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            spl::prep::SMEM_BYTES);
+        auto set = [](const void* f, int bytes) {
+            return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        };
+        attr_err = set((const void*)spl::prep_kernel<0, 0>, spl::prep::SMEM_BYTES);
+        if (attr_err == cudaSuccess) attr_err = set((const void*)spl::prep_kernel<1, 0>, spl::prep::SMEM_BYTES);
+        if (attr_err == cudaSuccess) attr_err = set((const void*)spl::prep_kernel<0, 1>, spl::prep::SMEM_BYTES);
+        if (attr_err == cudaSuccess) attr_err = set((const void*)spl::prep_kernel<1, 1>, spl::prep::SMEM_BYTES);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
@@ -1398,18 +1455,20 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     w.zero_v = (scan_flags & KDA_SCAN_ZERO_V) ? 1 : 0;
     w.wait_limit = wait_limit();
 
-    const uint64_t rowq = (uint64_t)a.H * spl::D;
+    const bool f32 = a.qkv_dtype == KDA_F32;
+    const uint32_t din = (uint32_t)a.dk;
+    const uint64_t rowq = (uint64_t)a.H * din;
     const uint64_t rows = (uint64_t)a.T_total;
     CUtensorMap mq, mk, mz, mv, mg, maw;
     cudaError_t e;
-    if ((e = make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, rowq, rows, spl::D, spl::C,
+    const CUtensorMapDataType tq = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const size_t eq = f32 ? 4 : 2;
+    if ((e = make_map(&mq, tq, eq, a.q, rowq, rows, din, spl::C, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, tq, eq, a.k, rowq, rows, din, spl::C, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
+    if ((e = make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, rowq, rows, din, spl::C,
                       CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k, rowq, rows, spl::D, spl::C,
-                      CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = make_map(&mz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.z, rowq, rows, spl::D, spl::C,
-                      CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.v, rowq, rows, 64, spl::C,
-                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, tq, eq, a.v, rowq, rows, f32 ? din : 64, spl::C,
+                      f32 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     constexpr int NE = spl::ScanCfg<spl::SCAN_R>::NE;
     if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, rowq, rows, NE, spl::C,
                       NE == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
@@ -1426,16 +1485,16 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
         if (L.nrec > 0) {
             const int nsm = spl::sm_count();
             const long grid = L.nrec < (long)(nsm > 0 ? nsm : 148) ? L.nrec : (long)(nsm > 0 ? nsm : 148);
-            if (a.gate_mode == KDA_GATE_SOFTPLUS)
-                spl::prep_kernel<1><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
-            else
-                spl::prep_kernel<0><<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            const bool sp = a.gate_mode == KDA_GATE_SOFTPLUS, f32 = a.qkv_dtype == KDA_F32;
+            auto kern = sp ? (f32 ? spl::prep_kernel<1, 1> : spl::prep_kernel<1, 0>)
+                           : (f32 ? spl::prep_kernel<0, 1> : spl::prep_kernel<0, 0>);
+            kern<<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
             ++launched;
         }
     }
     if (parts & 2) {
         dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
-        spl::scan_kernel<spl::SCAN_R><<<grid, spl::NT, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
+        spl::scan_kernel<spl::SCAN_R><<<grid, spl::ScanCfg<spl::SCAN_R>::NTS, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
         ++launched;
     }
     count_launches(launched);

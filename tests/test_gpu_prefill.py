@@ -41,9 +41,43 @@ def check(res, ref, tol_o=TOL_O, tol_s=TOL_S, bf16=True, seq_bounds=None):
 
 
 def test_tiny_fp32(kda_lib, cuda_dev):
+    """The tiny workload (T = 64, H = 1, d = 32, fp32, chunk 64 / sub-chunk 16)
+    through the chunked form: with its workspace kda_prefill runs the
+    chunk-parallel schedule (plan, prep, scan: three launches); the per-token
+    kernel (kda_prefill_recurrent) checks the same inputs."""
     import serving_kda_chunked_gated_gb300.kda as kda
     d = I.make_prefill(I.workload("tiny"))
-    check(run_gpu(kda, d, cuda_dev), run_oracle(d))
+    ref = run_oracle(d)
+    n0 = kda.launch_count()
+    res = run_gpu(kda, d, cuda_dev)
+    assert kda.launch_count() - n0 == 3            # plan + prep + scan: the chunked form ran
+    check(res, ref)
+    check(run_gpu(kda, d, cuda_dev, recurrent=True), ref)
+
+
+@pytest.mark.parametrize("dk", [32, 64])
+def test_fp32_small_d_chunked_ragged(kda_lib, cuda_dev, dk):
+    """float32 q, k, v with d = 32 and 64 on the chunk-parallel schedule: packed
+    ragged sequences (1, 63, 64, 65 and 200 tokens and an empty one), a prefix
+    state, snapshots every 64 tokens; against the oracle."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    cu = np.array([0, 1, 64, 64, 128, 193, 393], dtype=np.int32)
+    H = 2
+    d = I.make_prefill(I.workload("tiny", T=int(cu[-1]), H=H, dk=dk, dv=dk, S0_std=0.02, z_std=2.0, A_std=0.5))
+    d["cu_seqlens"] = cu
+    d["S0"] = (0.02 * np.random.default_rng(11).standard_normal((len(cu) - 1, H, dk, dk))).astype(np.float32)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    n0 = kda.launch_count()
+    o, S_T, y, snap = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev),
+                                  to_dev(d["A"], cuda_dev), cu_seqlens=to_dev(cu, cuda_dev),
+                                  S0=to_dev(d["S0"], cuda_dev), snap_interval=64)
+    torch.cuda.synchronize()
+    assert kda.launch_count() - n0 == 3
+    ro, rS, _, rsnap = oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"],
+                                      cu_seqlens=cu, S0=d["S0"], snap_interval=64)
+    parity("o", host(o), ro, TOL_O, seq_bounds=cu)
+    parity("S_T", host(S_T), rS, TOL_S, seq_bounds=range(len(cu)))
+    parity("snapshots", host(snap), rsnap, TOL_S)
 
 
 @pytest.mark.parametrize("T", [1, 15, 16, 64, 65, 300])
