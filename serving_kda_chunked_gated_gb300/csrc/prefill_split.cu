@@ -1106,8 +1106,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         // ------------------------------------------------------------------ epilogue
         // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
         // CTA's columns, and gamma_C[row]
-        float pu[HW], pg = 0.f;
-        auto load_rec = [&](int j) {
+        // Two register sets by chunk parity: the rows of chunk c are loaded in chunk
+        // c - 3 and stored into TMEM in chunk c - 1, so a load has two chunks to come
+        // back from DRAM (one chunk is close to the loaded DRAM's latency)
+        float pu0[HW], pu1[HW], pg0 = 0.f, pg1 = 0.f;
+        auto load_rec_to = [&](int j, float (&pu)[HW], float& pg) {
             const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
             if (!w.zero_v) {
 #pragma unroll
@@ -1115,13 +1118,20 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             }
             pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
         };
-        auto store_rec = [&](int b) {
+        auto load_rec = [&](int j) {   // into the set of chunk j's parity
+            if (j & 1) load_rec_to(j, pu1, pg1); else load_rec_to(j, pu0, pg0);
+        };
+        auto store_from = [&](int b, const float (&pu)[HW]) {
             if (!w.zero_v) {
 #pragma unroll
                 for (int i = 0; i < HW; i += 16)
                     tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
             }
         };
+        auto store_rec = [&](int j) {  // chunk j's rows into TMEM buffer j & 1; returns nothing
+            if (j & 1) store_from(1, pu1); else store_from(0, pu0);
+        };
+        auto gm_of = [&](int j) { return (j & 1) ? pg1 : pg0; };
         // o and y of chunk jo from its TMEM buffer (output-row threads)
         auto emit_outputs = [&](int jo) {
             const int bo = jo & 1;
@@ -1191,8 +1201,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int jj = 0; jj < 16; ++jj)
                     *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(v[jj]);
             }
-            if (nch > 0) { load_rec(0); store_rec(0); gm_next = pg; }
+            if (nch > 0) { load_rec(0); store_rec(0); gm_next = gm_of(0); }
             if (nch > 1) load_rec(1);
+            if (nch > 2) load_rec(2);
             tc::tmem_st_wait();
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -1231,8 +1242,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     else { ++n_full[b]; tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4); }
                 }
             }
-            if (j + 1 < nch) { store_rec(b ^ 1); gm_next = pg; }
-            if (j + 2 < nch) load_rec(j + 2);
+            if (j + 1 < nch) { store_rec(j + 1); gm_next = gm_of(j + 1); }
+            if (j + 3 < nch) load_rec(j + 3);   // into the set just stored from
             tc::tmem_st_wait();
             wait(bar_m2, j & 1);
             tc::fence_after_sync();
