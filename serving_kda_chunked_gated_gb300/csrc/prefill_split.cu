@@ -879,12 +879,6 @@ TC_DEV void st_async_f32(uint32_t addr, float v, uint32_t mbar_addr) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                  :: "r"(addr), "r"(__float_as_uint(v)), "r"(mbar_addr) : "memory");
 }
-// arrive on a peer CTA's mbarrier; release at CTA scope orders this CTA's earlier
-// shared-memory reads (gathered by a __syncwarp) before the peer's refill, and
-// unlike a cluster-scope release it does not wait for the thread's global traffic
-TC_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
-}
 TC_DEV void mbar_arrive_local(uint64_t* mbar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(tc::smem_u32(mbar)) : "memory");
 }
@@ -950,8 +944,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint64_t* bar_g = bars + 4;          // g_in tile of chunk j landed (phase j)
     uint64_t* bar_gfree = bars + 5;      // the output warps have read the g_in tile of chunk j
     uint64_t* bar_full = bars + 6;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
-    uint64_t* bar_free = bars + 8;       // [2][R] peer p has read this CTA's sums of chunk j
-    uint64_t* bar_k = bars + 8 + 2 * R;  // [2] (K gamma_C / Gamma)^T of chunk j landed in buffer j & 1
+    uint64_t* bar_k = bars + 8;          // [2] (K gamma_C / Gamma)^T of chunk j landed in buffer j & 1
     uint64_t* bar_awfree = bar_k + 2;    // [2] MMA 2 has read A-tile buffer b (one phase per use)
     uint64_t* bar_kfree = bar_awfree + 2;   // [2] MMA 3 has read K buffer b (one phase per use)
     uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_kfree + 2);
@@ -987,7 +980,6 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(bar_aw + b, 1);
             tc::mbar_init(bar_full + b, 1);
-            for (int p = 0; p < R; ++p) tc::mbar_init(bar_free + b * R + p, 4);   // peer p's output warps
             tc::mbar_init(bar_k + b, 1);
             tc::mbar_init(bar_awfree + b, 1);
             tc::mbar_init(bar_kfree + b, 1);
@@ -1224,14 +1216,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 if (j > 0 && (a.o || gate)) {
                     emit_outputs(j - 1);
                     if (gate) {
-                        // the g_in tile and the peers' sums of chunk j - 1 are read
+                        // the g_in tile of chunk j - 1 is read
                         __syncwarp();
-                        if (lane == 0) {
-                            mbar_arrive_local(bar_gfree);
-#pragma unroll
-                            for (int p = 1; p < R; ++p)
-                                mbar_arrive_remote(cluster_map(bar_free + (b ^ 1) * R + r, (r + p) % R));
-                        }
+                        if (lane == 0) mbar_arrive_local(bar_gfree);
                     }
                 }
                 // arm this chunk's exchange barrier (its phase for chunk j - 2 completed:
@@ -1276,15 +1263,14 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 ss *= a.scale * a.scale;
                 s_rowpart[(b * 2 + hf) * C + t] = ss;
                 nbar_sync(NB_O, NO);   // both halves of this chunk's sums are in s_rowpart
-                // the row's sum over this CTA's columns into every peer's s_rowsq[b] (by the
-                // first half's thread), once every peer has read what this CTA wrote there
-                // for chunk j - 2 (one barrier per peer: a peer's signals reach it in
-                // order, different peers' need not)
+                // the row's sum over this CTA's columns into every peer's s_rowsq[b], by the
+                // first half's thread.  What this CTA wrote there for chunk j - 2 has been
+                // read: every peer read it (emit_outputs of chunk j - 2, both halves, then
+                // the peer's NB_O) before it sent its sums of chunk j - 1, whose arrival
+                // this thread awaited in emit_outputs of chunk j - 1; the st.async
+                // complete-tx releases at cluster scope and that wait acquires at cluster
+                // scope, so each peer's reads happen before these writes.
                 if (hf == 0) {
-                    if (j >= 2) {
-#pragma unroll
-                        for (int p = 1; p < R; ++p) wait_cl(bar_free + b * R + (r + p) % R, ((j - 2) >> 1) & 1);
-                    }
                     const float own = ss + s_rowpart[(b * 2 + 1) * C + t];
                     if (!xdead) {
 #pragma unroll
