@@ -47,17 +47,20 @@ constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
 constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
 constexpr int SCAN_R = 4; // scan: CTAs (value-column blocks) per (sequence, head)
 
-// one record per (chunk, head), in four arrays of the workspace
-constexpr size_t AW_FLOATS = 128 * 128;   // [-W ; Gamma Q - P Gamma K]  [row][d]
-constexpr size_t UU_FLOATS = 128 * 128;   // [U ; U_o]                   [row][e]
-constexpr size_t KT_FLOATS = 128 * 64;    // (K gamma_C / Gamma)^T       [d][t]
-constexpr size_t GM_FLOATS = 128;         // gamma_C                     [d]
+// one record per (chunk, head), in four arrays of the workspace: the two MMA
+// operands in fp16 (the tf32 mantissa; their range is bounded, see the scan),
+// the additive terms and the decay in FP32
+constexpr size_t AW_ELEMS = 128 * 128;    // [-W ; Gamma Q - P Gamma K]  [row][d]  fp16
+constexpr size_t UU_FLOATS = 128 * 128;   // [U ; U_o]                   [row][e]  FP32
+constexpr size_t KT_ELEMS = 128 * 64;     // (K gamma_C / Gamma)^T       [d][t]    fp16
+constexpr size_t GM_FLOATS = 128;         // gamma_C                     [d]       FP32
 
 struct Work {
     const int* chunk_base;   // [num_seqs + 1] first global chunk of each sequence
-    float* aw;
+    int* vmax;               // [num_seqs][H][128] max |v| of each value column (FP32 bits)
+    uint16_t* aw;
     float* uu;
-    float* kt;
+    uint16_t* kt;
     float* gm;
     int* err;                // error word: tc::ERR_WAIT | tc::ERR_DRAIN
     long nrec;               // chunks * H
@@ -81,6 +84,15 @@ TC_DEV uint32_t sw128_bf16(int row, int col) {
     return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 TC_DEV float4 ld_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+// 2^e as a float, e in [-126, 127]
+TC_DEV float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+// 16 values as fp16 in one 32-byte streaming store (p 32-byte aligned)
+TC_DEV void st_stream_h16(uint16_t* p, const float* v) {
+    float w8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w8[i] = __uint_as_float(tc::pack_f16x2(v[2 * i], v[2 * i + 1]));
+    st_stream_f8(reinterpret_cast<float*>(p), w8);
+}
 // four 8 x 4 fp32 matrices from shared memory (ldmatrix on 16-bit pairs): lane l
 // passes the address of row l & 7 of matrix l >> 3 (16-byte aligned) and gets
 // word (l & 3) of row (l >> 2) of each matrix -- the tf32 m16n8k8 fragment order
@@ -93,7 +105,8 @@ TC_DEV void ldsm_x4(const float* p, uint32_t (&r)[4]) {
 // plan: chunk_base[n] = sum_{m < n} ceil(len_m / C), n = 0..num_seqs (one CTA);
 // also clears the call's error word
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs, int* chunk_base, int* err) {
+__global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs, int* chunk_base, int* vmax,
+                                                     long nvmax, int* err) {
     __shared__ int s_warp[32];
     __shared__ int s_carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -131,10 +144,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int* cu, int num_seqs,
         __syncthreads();
     }
     if (tid == 0) chunk_base[num_seqs] = s_carry;
+    for (long i = tid; i < nvmax; i += 1024) vmax[i] = 0;   // prep takes maxima into it
 }
 
 // record -> (sequence, first token, tokens, head); chunk_base has num_seqs + 1 entries
-struct Loc { int t0, nc, h; };
+struct Loc { int t0, nc, h, n; };
 TC_DEV Loc locate(long rec, int H, const int* cu, const int* cb, int num_seqs) {
     const int g = (int)(rec / H);
     Loc l;
@@ -146,6 +160,7 @@ TC_DEV Loc locate(long rec, int H, const int* cu, const int* cb, int num_seqs) {
     }
     l.t0 = cu[lo] + C * (g - cb[lo]);
     l.nc = min(C, cu[lo + 1] - l.t0);
+    l.n = lo;
     return l;
 }
 
@@ -268,7 +283,8 @@ prep_kernel(kda_prefill_args a, Work w,
     float* s_ctab = fs + SM_CTAB;
     float* s_diag = fs + SM_DIAG;
     float* s_eA = fs + SM_EA;
-    // s_loc: [0..2] this record's {t0, nc, h}, [3..5] the next one's; [8..15] the walk
+    // s_loc: [0..2] this record's {t0, nc, h}, [3..5] the next one's, [6], [7] their
+    // sequences; [8..15] the walk
     // at the next record: chunk g (long), head, sequence n, cb[n], cb[n+1], cu[n], cu[n+1]
     int* s_loc = reinterpret_cast<int*>(fs + SM_LOC);
     uint64_t* mbar = reinterpret_cast<uint64_t*>(fs + SM_FLOATS);
@@ -305,7 +321,7 @@ prep_kernel(kda_prefill_args a, Work w,
     const long step_g = stride / H;
     const int step_h = (int)(stride - step_g * H);
     if (tid == NTP - 1) {
-        s_loc[0] = cur.t0; s_loc[1] = cur.nc; s_loc[2] = cur.h;
+        s_loc[0] = cur.t0; s_loc[1] = cur.nc; s_loc[2] = cur.h; s_loc[6] = cur.n;
         const long rn = rec + stride;
         const long g = rn / H;
         const int hn = (int)(rn - g * H);
@@ -319,7 +335,7 @@ prep_kernel(kda_prefill_args a, Work w,
         s_loc[12] = w.chunk_base[n]; s_loc[13] = w.chunk_base[n + 1];
         s_loc[14] = a.cu_seqlens[n]; s_loc[15] = a.cu_seqlens[n + 1];
         const int t0 = s_loc[14] + C * (int)(g - s_loc[12]);
-        s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hn;
+        s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hn; s_loc[7] = n;
     }
     // thread 0 issues every copy and MMA; it counts the phases it issued on each
     // mbarrier, for the give-up path at the end
@@ -356,8 +372,8 @@ prep_kernel(kda_prefill_args a, Work w,
 
     for (; rec < w.nrec; rec += stride) {
         const bool has_next = rec + stride < w.nrec;
-        cur = Loc{s_loc[0], s_loc[1], s_loc[2]};
-        const Loc nxt = has_next ? Loc{s_loc[3], s_loc[4], s_loc[5]} : cur;
+        cur = Loc{s_loc[0], s_loc[1], s_loc[2], s_loc[6]};
+        const Loc nxt = has_next ? Loc{s_loc[3], s_loc[4], s_loc[5], s_loc[7]} : cur;
         const int nc = cur.nc, h = cur.h;
         const float eA = h < EA_HEADS ? s_eA[h] : __expf(__ldg(a.A + h));
         if (tid < C) {
@@ -509,15 +525,11 @@ prep_kernel(kda_prefill_args a, Work w,
                     *reinterpret_cast<float*>(sKV + tc::sw128_offset(r0 + i, d, KV_ROWS)) = tc::to_tf32(kf2[i] * cf);
             }
             // the record's (K gamma_C / Gamma)^T: row d, the 16 tokens of sub-chunk b
-            float* dst = w.kt + rec * KT_FLOATS + (size_t)d * C + 16 * b;
             const float ec = s_expCE[b * D + d];
+            float k16[16];
 #pragma unroll
-            for (int t = 0; t < 16; t += 8) {
-                float k8[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) k8[u] = tc::to_tf32(kf2[t + u] * ec);
-                st_stream_f8(dst + t, k8);
-            }
+            for (int u = 0; u < 16; ++u) k16[u] = kf2[u] * ec;
+            st_stream_h16(w.kt + rec * KT_ELEMS + (size_t)d * C + 16 * b, k16);
             tc::fence_proxy_async();
         }
         __syncthreads();
@@ -703,14 +715,21 @@ prep_kernel(kda_prefill_args a, Work w,
             const int rr = tid & (2 * D - 1), th = tid >> 8;   // B_pre row, half of the tokens
             if (rr < D) {                        // rows 0..127: value columns
                 const int e = rr;
+                float vm = 0.f;   // max |v| of this column over the half's tokens
 #pragma unroll 4
                 for (int t = 32 * th; t < 32 * th + 32; t += 4) {
                     float4 w4;
                     float* wp = &w4.x;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) wp[u] = (t + u < nc) ? raw_v(t + u, e) : 0.f;
+                    for (int u = 0; u < 4; ++u) {
+                        wp[u] = (t + u < nc) ? raw_v(t + u, e) : 0.f;
+                        vm = fmaxf(vm, fabsf(wp[u]));
+                    }
                     *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, 2 * D)) = w4;
                 }
+                // the sequence's column maximum, for the scan's operand scaling
+                // (non-negative floats order like their bit patterns)
+                if (vm > 0.f) atomicMax(w.vmax + ((size_t)cur.n * H + h) * D + e, __float_as_int(vm));
                 if (th == 0) w.gm[rec * GM_FLOATS + e] = s_gam[e];
             } else {                             // rows 128..255: (Gamma K)^T
                 const int d = rr - D;
@@ -761,7 +780,7 @@ prep_kernel(kda_prefill_args a, Work w,
         {
             float v[16];
             float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 32 * grp;
-            float* aw = w.aw + rec * AW_FLOATS + (size_t)row * D + 32 * grp;
+            uint16_t* aw = w.aw + rec * AW_ELEMS + (size_t)row * D + 32 * grp;
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
@@ -775,9 +794,8 @@ prep_kernel(kda_prefill_args a, Work w,
                     tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(-v[j]);
-                    st_stream_f8(aw + c, v);
-                    st_stream_f8(aw + c + 8, v + 8);
+                    for (int j = 0; j < 16; ++j) v[j] = -v[j];
+                    st_stream_h16(aw + c, v);
                 }
             } else {
                 const int t = row - C;
@@ -792,19 +810,18 @@ prep_kernel(kda_prefill_args a, Work w,
                         const int d = 32 * grp + c + j;
                         const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
                         const float4 e4 = *reinterpret_cast<const float4*>(es + d);
-                        o4[j] = tc::to_tf32(q4.x * e4.x - v[j]);
-                        o4[j + 1] = tc::to_tf32(q4.y * e4.y - v[j + 1]);
-                        o4[j + 2] = tc::to_tf32(q4.z * e4.z - v[j + 2]);
-                        o4[j + 3] = tc::to_tf32(q4.w * e4.w - v[j + 3]);
+                        o4[j] = q4.x * e4.x - v[j];
+                        o4[j + 1] = q4.y * e4.y - v[j + 1];
+                        o4[j + 2] = q4.z * e4.z - v[j + 2];
+                        o4[j + 3] = q4.w * e4.w - v[j + 3];
                     }
-                    st_stream_f8(aw + c, o4);
-                    st_stream_f8(aw + c + 8, o4 + 8);
+                    st_stream_h16(aw + c, o4);
                 }
             }
             tc::fence_before_sync();
         }
         if (tid == NTP - 1 && has_next) {   // advance the walk: this record <- the next, next <- one stride on
-            s_loc[0] = s_loc[3]; s_loc[1] = s_loc[4]; s_loc[2] = s_loc[5];
+            s_loc[0] = s_loc[3]; s_loc[1] = s_loc[4]; s_loc[2] = s_loc[5]; s_loc[6] = s_loc[7];
             long g = *reinterpret_cast<const long*>(s_loc + 8) + step_g;
             int hh = s_loc[10] + step_h;
             if (hh >= H) { hh -= H; ++g; }
@@ -817,7 +834,7 @@ prep_kernel(kda_prefill_args a, Work w,
                     s_loc[14] = a.cu_seqlens[n]; s_loc[15] = a.cu_seqlens[n + 1];
                 }
                 const int t0 = s_loc[14] + C * (int)(g - s_loc[12]);
-                s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hh;
+                s_loc[3] = t0; s_loc[4] = min(C, s_loc[15] - t0); s_loc[5] = hh; s_loc[7] = s_loc[11];
             }
             *reinterpret_cast<long*>(s_loc + 8) = g;
             s_loc[10] = hh;
@@ -847,21 +864,26 @@ template <int R>
 struct ScanCfg {
     static constexpr int NE = D / R;
     static constexpr int WARP_MMA = 8, WARP_LOAD = 9, NTS = 320;
-    static constexpr int AW_TILE = 128 * 128 * 4;            // SW128 [128 rows][128 K]
+    // MMA operands in fp16, SW128 K-major
+    static constexpr int AW_TILE = 128 * 128 * 2;            // [128 rows][128 K]
     static constexpr int OFF_AW0 = 0;
     static constexpr int OFF_AW1 = AW_TILE;
-    static constexpr int OFF_SOP = 2 * AW_TILE;              // S operand, SW128 [e][d]
-    static constexpr int OFF_VOP = OFF_SOP + NE * D * 4;     // V' operand, SW128 [e][t]
+    static constexpr int OFF_SOP = 2 * AW_TILE;              // S operand [e][d]
+    static constexpr int OFF_VOP = OFF_SOP + NE * D * 2;     // V' operand [e][t]
     static constexpr int G_TILE = C * NE * 2;                // g_in tile, [C][NE] bf16
-    static constexpr int OFF_G = OFF_VOP + NE * C * 4;
-    static constexpr int KT_BYTES = 128 * C * 4;             // (K gamma_C / Gamma)^T, SW128 [128 rows][C]
+    static constexpr int OFF_G = OFF_VOP + NE * C * 2;
+    static constexpr int KT_BYTES = 128 * C * 2;             // (K gamma_C / Gamma)^T [128 rows][C]
     static constexpr int OFF_K0 = OFF_G + G_TILE;            // MMA 3's A operand, one buffer per chunk parity
     static constexpr int OFF_K1 = OFF_K0 + KT_BYTES;
     static constexpr int OFF_SMALL = OFF_K1 + KT_BYTES;
     // small region (floats): peers' row sums of squares [2 parity][R source][C], this
-    // CTA's half-row sums [2 parity][2 half][C], RMSNorm weights of this CTA's columns [NE]
+    // CTA's half-row sums [2 parity][2 half][C], RMSNorm weights of this CTA's columns
+    // [NE], the columns' scale factors 2^-c and 2^c [NE each], the columns' largest
+    // |S0| [NE] (ints), the state warps' largest |S| [8] (ints)
     static constexpr int SM_ROWSQ = 0, SM_ROWPART = 2 * R * C, SM_NORMW = SM_ROWPART + 4 * C;
-    static constexpr int SM_FLOATS = SM_NORMW + NE;
+    static constexpr int SM_VSC = SM_NORMW + NE, SM_VINV = SM_VSC + NE, SM_CMAX = SM_VINV + NE;
+    static constexpr int SM_WMAX = SM_CMAX + NE;
+    static constexpr int SM_FLOATS = SM_WMAX + 8;
     static constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 256 + 1024;
     static constexpr uint32_t TM_D = 0;                      // 2 x NE cols: [U ; U_o] -> [V' ; O]
     static constexpr uint32_t TM_DS = 2 * NE;                // NE cols: state increment
@@ -918,14 +940,16 @@ TC_DEV uint32_t gtile_offset(int row, int col) {
 // squares, and o, y of chunk j are written during chunk j+1's MMA 2 from the TMEM
 // buffer that still holds them.  The R CTAs' row sums meet in each peer's shared
 // memory through st.async on mbarriers.
-template <int R>
+// TRANS: a transition scan (v = 0, the KCP pairs' M): the state exponent x follows
+// the state; otherwise x = 0
+template <int R, bool TRANS>
 __global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(ScanCfg<R>::NTS, 1)
 scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
             const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_kt) {
     using Cfg = ScanCfg<R>;
     constexpr int NE = Cfg::NE;
     constexpr int HW = NE / 2;           // value columns per epilogue thread
-    constexpr int NB_V = 1, NB_S = 2, NB_O = 3;   // named barriers
+    constexpr int NB_V = 1, NB_S = 2, NB_O = 3, NB_X = 4;   // named barriers
     constexpr int NV = 5 * 32;           // V' warps (0, 1, 4, 5) + the MMA warp
     constexpr int NS = 9 * 32;           // epilogue warps + the MMA warp
     constexpr int NO = 4 * 32;           // output-row warps (2, 3, 6, 7)
@@ -937,6 +961,24 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     float* s_rowsq = fs + Cfg::SM_ROWSQ;      // [2][R][C] peers' row sums, by parity and source
     float* s_rowpart = fs + Cfg::SM_ROWPART;  // [2][2][C] this CTA's, by parity and half
     float* s_normw = fs + Cfg::SM_NORMW;      // [NE] RMSNorm weights (ones without norm_w)
+    // The fp16 operands S and V' have the tf32 mantissa but a narrower range.  The
+    // recurrence is linear in (v, S0) column by column, so the scan carries column e of
+    // S, V', U and U_o (in TMEM and in the operands) times 2^(x_j - c_e), and only the
+    // boundary (S0, U in; o, S_T, snapshots out) rescales, by exact powers of two.
+    // 2^c_e is the power of two just above the column's largest |v| (the state then
+    // stays near 1), raised if needed to keep the largest |S0| below 2^12: content at
+    // the scale of v keeps the full fp16 mantissa while |S0| / |v| < 2^26.  A column
+    // with v = 0 takes 2^c_e from S0 alone.  In a transition scan (TRANS: v = 0, the
+    // state only decays or mixes) x_j, one exponent for the CTA's columns, follows
+    // the largest |S| chunk by chunk, so that the state's fp16 copy stays near 1
+    // however fast it decays; otherwise x_j = 0.  (Terms below 2^-24 of the record
+    // operands' own scale -- a chunk's contraction terms under very fast decay --
+    // are lost to fp16 whatever x: a transition matrix is exact to about 2^-24 of
+    // |S0|, not relative to itself once it has decayed below that.)
+    float* s_vsc = fs + Cfg::SM_VSC;          // [NE] 2^-c
+    float* s_vinv = fs + Cfg::SM_VINV;        // [NE] 2^c
+    int* s_cmax = reinterpret_cast<int*>(fs + Cfg::SM_CMAX);  // [NE] largest |S0|
+    uint32_t* s_wmax = reinterpret_cast<uint32_t*>(fs + Cfg::SM_WMAX);  // [8] per state warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(fs + Cfg::SM_FLOATS);
     uint64_t* bar_m2 = bars;             // MMA 2 of chunk j done (phase j)
     uint64_t* bar_m3 = bars + 1;         // MMA 3 of chunk j done (phase j)
@@ -971,7 +1013,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint8_t* sG = sm + Cfg::OFF_G;
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
-    if (tid < NE) s_normw[tid] = a.norm_w ? a.norm_w[NE * r + tid] : 1.f;
+    const int vmx = (tid < NE && !w.zero_v) ? w.vmax[((size_t)n * H + h) * D + NE * r + tid] : 0;
+    if (tid < NE) {
+        s_normw[tid] = a.norm_w ? a.norm_w[NE * r + tid] : 1.f;
+        s_cmax[tid] = 0;
+    }
     if (tid == 0) {
         tc::mbar_init(bar_m2, 1);
         tc::mbar_init(bar_m3, 1);
@@ -989,6 +1035,26 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if (a.S0) {   // the columns' largest |S0|
+        for (int i = tid; i < din * NE; i += Cfg::NTS) {
+            const int d = i / NE, c = i - d * NE;
+            if (NE * r + c < din)
+                atomicMax(s_cmax + c, __float_as_int(fabsf(a.S0[(((size_t)n * H + h) * din + d) * din + NE * r + c])));
+        }
+    }
+    __syncthreads();
+    if (tid < NE) {   // m = f 2^ex with f in [1/2, 1)
+        const float ms = __int_as_float(s_cmax[tid]), mv = __int_as_float(vmx);
+        const bool hs = ms > 0.f && ms <= 3.0e38f, hv = mv > 0.f && mv <= 3.0e38f;
+        int es = 0, ev = 0;
+        if (hs) frexpf(ms, &es);
+        if (hv) frexpf(mv, &ev);
+        int ex = hv ? (hs ? max(ev, es - 12) : ev) : es;
+        ex = max(-120, min(120, ex));
+        s_vsc[tid] = ldexpf(1.f, -ex);
+        s_vinv[tid] = ldexpf(1.f, ex);
+    }
+    __syncthreads();
     const uint32_t T0 = *tbase_ptr;
     if (gate) cluster_sync_all();   // every peer's mbarriers are initialised before the first remote access
 
@@ -1023,21 +1089,19 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 const int b = j & 1;
                 ++n_aw[b];
                 tc::mbar_arrive_expect_tx(bar_aw + b, Cfg::AW_TILE);
-                for (int s = 0; s < 4; ++s)
-                    tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 4), &tm_aw, 32 * s, (int)(rec_of(j) * 128), bar_aw + b);
+                for (int s = 0; s < 2; ++s)   // two 64-column slabs
+                    tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 2), &tm_aw, 64 * s, (int)(rec_of(j) * 128), bar_aw + b);
             };
             auto load_g = [&](int j) {
                 ++n_g;
                 tc::mbar_arrive_expect_tx(bar_g, Cfg::G_TILE);
                 tc::tma_load_2d(sG, &tm_g, h * D + NE * r, t_begin + C * j, bar_g);
             };
-            auto load_k = [&](int j) {   // both 32-token halves of chunk j's K^T
+            auto load_k = [&](int j) {   // chunk j's K^T: one 64-token slab
                 const int b = j & 1;
                 ++n_k[b];
                 tc::mbar_arrive_expect_tx(bar_k + b, Cfg::KT_BYTES);
-                for (int hh = 0; hh < 2; ++hh)
-                    tc::tma_load_2d(k_buf(b) + hh * (Cfg::KT_BYTES / 2), &tm_kt, 32 * hh, (int)(rec_of(j) * 128),
-                                    bar_k + b);
+                tc::tma_load_2d(k_buf(b), &tm_kt, 0, (int)(rec_of(j) * 128), bar_k + b);
             };
             for (int j = 0; j < 2 && j < nch; ++j) { load_aw(j); load_k(j); }
             if (gate && nch > 0) load_g(0);
@@ -1065,10 +1129,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     const uint32_t ab = tc::smem_u32(aw_buf(b));
                     const uint32_t sb = tc::smem_u32(sSop);
 #pragma unroll
-                    for (int ks = 0; ks < D / 8; ++ks)
-                        tc::mma_tf32_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks),
-                                        tc::sw128_desc_k(sb, NE, ks), tc::idesc_tf32(128, NE),
-                                        (ks > 0 || !w.zero_v) ? 1u : 0u);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc::mma_f16_ss(T0 + Cfg::TM_D + NE * b, tc::sw128_desc_k(ab, 128, ks),
+                                       tc::sw128_desc_k(sb, NE, ks), tc::idesc_f16(128, NE),
+                                       (ks > 0 || !w.zero_v) ? 1u : 0u);
                     ++n_m2;
                     tc::mma_commit(bar_m2);
                     ++n_awf[b];
@@ -1083,9 +1147,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 const uint32_t kb = tc::smem_u32(k_buf(b));
                 const uint32_t vb = tc::smem_u32(sVop);
 #pragma unroll
-                for (int ks = 0; ks < C / 8; ++ks)
-                    tc::mma_tf32_ss(T0 + Cfg::TM_DS, tc::sw128_desc_k(kb, 128, ks), tc::sw128_desc_k(vb, NE, ks),
-                                    tc::idesc_tf32(128, NE), ks > 0);
+                for (int ks = 0; ks < C / 16; ++ks)
+                    tc::mma_f16_ss(T0 + Cfg::TM_DS, tc::sw128_desc_k(kb, 128, ks), tc::sw128_desc_k(vb, NE, ks),
+                                   tc::idesc_f16(128, NE), ks > 0);
                 ++n_m3;
                 tc::mma_commit(bar_m3);
                 ++n_kf[b];
@@ -1113,19 +1177,23 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         auto load_rec = [&](int j) {   // into the set of chunk j's parity
             if (j & 1) load_rec_to(j, pu1, pg1); else load_rec_to(j, pu0, pg0);
         };
-        auto store_from = [&](int b, const float (&pu)[HW]) {
+        auto store_from = [&](int b, const float (&pu)[HW]) {   // scaled by 2^-c (x = 0 with U)
             if (!w.zero_v) {
 #pragma unroll
-                for (int i = 0; i < HW; i += 16)
-                    tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, pu + i);
+                for (int i = 0; i < HW; i += 16) {
+                    float v[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] = pu[i + k] * s_vsc[c_lo + i + k];
+                    tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, v);
+                }
             }
         };
-        auto store_rec = [&](int j) {  // chunk j's rows into TMEM buffer j & 1; returns nothing
+        auto store_rec = [&](int j) {  // chunk j's rows into TMEM buffer j & 1
             if (j & 1) store_from(1, pu1); else store_from(0, pu0);
         };
         auto gm_of = [&](int j) { return (j & 1) ? pg1 : pg0; };
         // o and y of chunk jo from its TMEM buffer (output-row threads)
-        auto emit_outputs = [&](int jo) {
+        auto emit_outputs = [&](int jo, int xo) {   // xo: the chunk's exponent
             const int bo = jo & 1;
             const int t = row - C;
             const int c0o = t_begin + C * jo;
@@ -1135,7 +1203,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             for (int c = 0; c < HW; c += 16) tc::tmem_ld16(T0 + Cfg::TM_D + NE * bo + lane_base + c_lo + c, o + c);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < HW; ++c) o[c] *= a.scale;
+            for (int c = 0; c < HW; ++c) o[c] *= a.scale * s_vinv[c_lo + c] * exp2i(-xo);
             if (t < nco && a.o) {
                 if (din == D) {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
@@ -1177,8 +1245,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             }
         };
 
-        // ---- initial state -> TMEM master copy and the tf32 operand copy
+        // ---- initial state -> TMEM master copy and the fp16 operand copy
         float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
+        int x_prev = 0, x_cur = 0, x_next = 0;   // the exponent x of the previous, this, the next chunk
         {
             const int d = row;
             const size_t sb = (((size_t)n * H + h) * din + d) * din + NE * r;
@@ -1187,11 +1256,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             for (int c = c_lo; c < c_lo + HW; c += 16) {
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
-                    v[jj] = (a.S0 && d < din && NE * r + c + jj < din) ? a.S0[sb + c + jj] : 0.f;
+                    v[jj] = (a.S0 && d < din && NE * r + c + jj < din) ? a.S0[sb + c + jj] * s_vsc[c + jj] : 0.f;
                 tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, v);
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
-                    *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(v[jj]);
+                    *reinterpret_cast<uint16_t*>(sSop + tc::sw128_offset_h(c + jj, d, NE)) = tc::f32_to_f16(v[jj]);
             }
             if (nch > 0) { load_rec(0); store_rec(0); gm_next = gm_of(0); }
             if (nch > 1) load_rec(1);
@@ -1214,7 +1283,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             //      after it into registers
             if (!vrow) {
                 if (j > 0 && (a.o || gate)) {
-                    emit_outputs(j - 1);
+                    emit_outputs(j - 1, x_prev);
                     if (gate) {
                         // the g_in tile of chunk j - 1 is read
                         __syncwarp();
@@ -1245,7 +1314,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        *reinterpret_cast<float*>(sVop + tc::sw128_offset(c + jj, t, NE)) = tc::to_tf32(v[jj]);
+                        *reinterpret_cast<uint16_t*>(sVop + tc::sw128_offset_h(c + jj, t, NE)) = tc::f32_to_f16(v[jj]);
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
@@ -1258,7 +1327,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) ss = fmaf(v[jj], v[jj], ss);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float x = v[jj] * (s_vinv[c + jj] * exp2i(-x_cur));
+                        ss = fmaf(x, x, ss);
+                    }
                 }
                 ss *= a.scale * a.scale;
                 s_rowpart[(b * 2 + hf) * C + t] = ss;
@@ -1281,8 +1353,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 }
             }
 
-            // ---- S = Diag(gamma_C) S + dS (FP32 in TMEM), refresh the tf32 operand copy;
-            //      a chunk that closes a prefix-cache interval also writes S out
+            // ---- S = Diag(gamma_C) S + dS (FP32 in TMEM), refresh the fp16 operand copy
+            //      (in a transition scan first moved to the next chunk's exponent); a
+            //      chunk that closes a prefix-cache interval also writes S out
             wait(bar_m3, j & 1);
             tc::fence_after_sync();
             {
@@ -1293,36 +1366,69 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                                       (c0 + nc - t_begin) / a.snap_interval - 1;
                     snap = a.S_snap + ((srow * H + h) * din + d) * din + NE * r;
                 }
+                static_assert(HW == 16, "one 16-column group per state thread");
                 float dv[16], sv[16];
+                const int c = c_lo;
+                tc::tmem_ld16(T0 + Cfg::TM_DS + lane_base + c, dv);
+                tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, sv);
+                tc::tmem_ld_wait();
 #pragma unroll
-                for (int c = c_lo; c < c_lo + HW; c += 16) {
-                    tc::tmem_ld16(T0 + Cfg::TM_DS + lane_base + c, dv);
-                    tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, sv);
-                    tc::tmem_ld_wait();
+                for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
+                x_next = x_cur;
+                if (TRANS) {
+                    // the largest |S| over the CTA's state warps (non-negative floats
+                    // order like their bit patterns) brings x back to [1/2, 1) when it
+                    // left [2^-6, 2^6)
+                    float mx = 0.f;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) sv[jj] = fmaf(gm, sv[jj], dv[jj]);
-                    tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, sv);
-                    if (snap && din == D) {
+                    for (int jj = 0; jj < 16; ++jj) mx = fmaxf(mx, fabsf(sv[jj]));
+                    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(mx));
+                    if (lane == 0) s_wmax[warp] = wm;
+                    nbar_sync(NB_X, 8 * 32);
+                    uint32_t m8 = 0;
 #pragma unroll
-                        for (int jj = 0; jj < 16; jj += 4)
-                            *reinterpret_cast<float4*>(snap + c + jj) = make_float4(sv[jj], sv[jj + 1], sv[jj + 2], sv[jj + 3]);
-                    } else if (snap && d < din) {
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (NE * r + c + jj < din) snap[c + jj] = sv[jj];
+                    for (int k = 0; k < 8; ++k) m8 = max(m8, s_wmax[k]);
+                    const float m = __uint_as_float(m8);
+                    if (m > 0.f && m <= 3.0e38f) {
+                        int ex;
+                        frexpf(m, &ex);
+                        if (ex < -5 || ex > 6) x_next = max(-100, min(100, x_cur - max(-60, min(60, ex))));
                     }
+                    const float px = exp2i(x_next - x_cur);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) sv[jj] *= px;
+                }
+                const float pu = exp2i(-x_next);
+                {
+                    tc::tmem_st16(T0 + Cfg::TM_S + lane_base + c, sv);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        *reinterpret_cast<float*>(sSop + tc::sw128_offset(c + jj, d, NE)) = tc::to_tf32(sv[jj]);
+                        *reinterpret_cast<uint16_t*>(sSop + tc::sw128_offset_h(c + jj, d, NE)) = tc::f32_to_f16(sv[jj]);
+                    if (snap) {
+                        float su[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) su[jj] = sv[jj] * (s_vinv[c + jj] * pu);
+                        if (din == D) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; jj += 4)
+                                *reinterpret_cast<float4*>(snap + c + jj) = make_float4(su[jj], su[jj + 1], su[jj + 2], su[jj + 3]);
+                        } else if (d < din) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj)
+                                if (NE * r + c + jj < din) snap[c + jj] = su[jj];
+                        }
+                    }
                 }
                 tc::tmem_st_wait();
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
             }
             nbar_sync(NB_S, NS);
+            x_prev = x_cur;
+            x_cur = x_next;
         }
         // outputs of the last chunk
-        if (nch > 0 && !vrow && (a.o || gate)) emit_outputs(nch - 1);
+        if (nch > 0 && !vrow && (a.o || gate)) emit_outputs(nch - 1, x_prev);
 
         // ---- final state
         if (a.S_T) {
@@ -1333,6 +1439,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             for (int c = c_lo; c < c_lo + HW; c += 16) {
                 tc::tmem_ld16(T0 + Cfg::TM_S + lane_base + c, v);
                 tc::tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) v[jj] *= s_vinv[c + jj] * exp2i(-x_cur);
                 if (din == D) {
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4)
@@ -1383,18 +1491,21 @@ static long total_chunks(const kda_prefill_args& a) {
     return c;
 }
 
-// workspace: error word at 0, chunk offsets at 256, then the record arrays from
-// the first 1024-byte aligned address after them (the size allows for the slack)
-struct Layout { size_t base, rec_start, aw, uu, kt, gm, total; long nrec; };
+// workspace: error word at 0, chunk offsets at 256, the value-column maxima,
+// then the record arrays from the first 1024-byte aligned address after them
+// (the size allows for the slack)
+struct Layout { size_t base, vmax, rec_start, aw, uu, kt, gm, total; long nrec, nvmax; };
 static Layout layout(const kda_prefill_args& a) {
     Layout l;
     l.nrec = total_chunks(a) * a.H;
+    l.nvmax = (long)a.num_seqs * a.H * D;
     l.base = 256;
-    l.rec_start = l.base + 4 * (size_t)(a.num_seqs + 1);
+    l.vmax = align_up(l.base + 4 * (size_t)(a.num_seqs + 1), 16);
+    l.rec_start = l.vmax + 4 * (size_t)l.nvmax;
     l.aw = 0;                                               // relative to the aligned record start
-    l.uu = l.aw + (size_t)l.nrec * AW_FLOATS * 4;
+    l.uu = l.aw + (size_t)l.nrec * AW_ELEMS * 2;
     l.kt = l.uu + (size_t)l.nrec * UU_FLOATS * 4;
-    l.gm = l.kt + (size_t)l.nrec * KT_FLOATS * 4;
+    l.gm = l.kt + (size_t)l.nrec * KT_ELEMS * 2;
     l.total = l.rec_start + 1024 + l.gm + (size_t)l.nrec * GM_FLOATS * 4;
     return l;
 }
@@ -1433,8 +1544,11 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
         if (attr_err == cudaSuccess) attr_err = set((const void*)spl::prep_kernel<0, 1>, spl::prep::SMEM_BYTES);
         if (attr_err == cudaSuccess) attr_err = set((const void*)spl::prep_kernel<1, 1>, spl::prep::SMEM_BYTES);
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
+            attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R, false>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(spl::scan_kernel<spl::SCAN_R, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
     if (a.num_seqs == 0) return cudaSuccess;
@@ -1444,9 +1558,10 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     w.err = reinterpret_cast<int*>(ws);
     w.chunk_base = reinterpret_cast<const int*>(ws + L.base);
     uint8_t* recs = reinterpret_cast<uint8_t*>(spl::align_up(reinterpret_cast<uintptr_t>(ws) + L.rec_start, 1024));
-    w.aw = reinterpret_cast<float*>(recs + L.aw);
+    w.vmax = reinterpret_cast<int*>(ws + L.vmax);
+    w.aw = reinterpret_cast<uint16_t*>(recs + L.aw);
     w.uu = reinterpret_cast<float*>(recs + L.uu);
-    w.kt = reinterpret_cast<float*>(recs + L.kt);
+    w.kt = reinterpret_cast<uint16_t*>(recs + L.kt);
     w.gm = reinterpret_cast<float*>(recs + L.gm);
     w.nrec = L.nrec;
     w.zero_v = (scan_flags & KDA_SCAN_ZERO_V) ? 1 : 0;
@@ -1469,15 +1584,16 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     constexpr int NE = spl::ScanCfg<spl::SCAN_R>::NE;
     if ((e = make_map(&mg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.g_in ? a.g_in : a.v, rowq, rows, NE, spl::C,
                       NE == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
-    if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.aw, 128, (uint64_t)L.nrec * 128, 32, 128,
+    if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.aw, 128, (uint64_t)L.nrec * 128, 64, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     CUtensorMap mkt;
-    if ((e = make_map(&mkt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.kt, spl::C, (uint64_t)L.nrec * 128, 32, 128,
+    if ((e = make_map(&mkt, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.kt, spl::C, (uint64_t)L.nrec * 128, 64, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
 
     int launched = 0;
     if (parts & 1) {
-        spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base), w.err);
+        spl::plan_kernel<<<1, 1024, 0, s>>>(a.cu_seqlens, a.num_seqs, const_cast<int*>(w.chunk_base), w.vmax,
+                                             L.nvmax, w.err);
         ++launched;
         if (L.nrec > 0) {
             const int nsm = spl::sm_count();
@@ -1491,7 +1607,8 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     }
     if (parts & 2) {
         dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
-        spl::scan_kernel<spl::SCAN_R><<<grid, spl::ScanCfg<spl::SCAN_R>::NTS, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
+        auto kern = w.zero_v ? spl::scan_kernel<spl::SCAN_R, true> : spl::scan_kernel<spl::SCAN_R, false>;
+        kern<<<grid, spl::ScanCfg<spl::SCAN_R>::NTS, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
         ++launched;
     }
     count_launches(launched);

@@ -4,8 +4,8 @@
 // the warp-level mma.sync used for 16x16 sub-blocks.
 //
 // Shared-memory operand layout used everywhere ("SW128 K-major"): an R x K
-// operand (R rows = M or N, K = reduction dim, 4-byte elements) is stored as
-// K/32 slabs of R rows x 128 bytes; row r of a slab sits at
+// operand (R rows = M or N, K = reduction dim) is stored as slabs of R rows x
+// 128 bytes (32 four-byte or 64 two-byte elements of K per slab); row r of a slab sits at
 // (r/8)*1024 + (r%8)*128 and its 16-byte chunk c is stored at chunk c ^ (r%8)
 // (the 128-byte swizzle), so slabs must be 1024-byte aligned.
 #pragma once
@@ -25,6 +25,14 @@ TC_DEV uint32_t sw128_offset(int r, int k, int R) {
                       ((((kk >> 2) ^ (r & 7)) << 4)) + ((kk & 3) << 2));
 }
 
+// byte offset of 2-byte element (r, k) inside an SW128 K-major operand with R rows
+// (slabs of 64 elements)
+TC_DEV uint32_t sw128_offset_h(int r, int k, int R) {
+    const int slab = k >> 6, kk = k & 63;
+    return (uint32_t)(slab * R * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                      ((((kk >> 3) ^ (r & 7)) << 4)) + ((kk & 7) << 1));
+}
+
 // Shared-memory matrix descriptor for an SW128 K-major operand; `addr` is the
 // shared address of element (0, k0) (k0 a multiple of 8 for 4-byte types).
 TC_DEV uint64_t sw128_desc(uint32_t addr) {
@@ -37,7 +45,8 @@ TC_DEV uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
-// descriptor for k-step `ks` (8 tf32 elements each) of an SW128 K-major operand
+// descriptor for k-step `ks` of an SW128 K-major operand: 32 bytes per step, i.e.
+// 8 tf32 elements (kind::tf32) or 16 fp16 elements (kind::f16)
 TC_DEV uint64_t sw128_desc_k(uint32_t base, int R, int ks) {
     const int k0 = ks * 8;
     return sw128_desc(base + (uint32_t)((k0 >> 5) * R * 128 + (k0 & 31) * 4));
@@ -50,6 +59,25 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool neg_a = fal
          | ((neg_a ? 1u : 0u) << 13)
          | ((uint32_t)(N >> 3) << 17)
          | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with fp16 A and B, FP32 accumulate, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4)                 // D = F32 (A, B = F16: format 0)
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
+// FP32 -> FP16 (round to nearest even): one value, and a pair packed as (lo, hi)
+TC_DEV uint16_t f32_to_f16(float x) {
+    uint16_t h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(x));
+    return h;
+}
+TC_DEV uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // ---------------------------------------------------------------------------
@@ -87,6 +115,13 @@ TC_DEV void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint3
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
         :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
+}
+TC_DEV void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc) : "memory");
 }
 // arrive on an mbarrier once all previously issued MMAs of this thread complete
 TC_DEV void mma_commit(uint64_t* mbar) {

@@ -37,10 +37,18 @@ def test_pair_from_state_only_prefills(kda_lib, cuda_dev):
     qn = f64(d, "q")
     kn = f64(d, "k")
     kn = kn / np.sqrt((kn * kn).sum(-1, keepdims=True) + 1e-6)   # the prefill's L2Norm of k
+    X = 0.02 * np.random.default_rng(7).standard_normal((128, 128))   # a state of the workload's scale
     for h in range(2):
         g = oracle.log_decay(d["z"][:, h], d["A"][h])
         rM, rSt = chunked.kcp_pair(kn[:, h], f64(d, "v")[:, h], g, d["beta"][:, h].astype(np.float64))
-        assert rel(host(M[h]), rM) < TOL_S and rel(host(St[h]), rSt) < TOL_S
+        assert rel(host(St[h]), rSt) < TOL_S
+        # the fold the pair exists for: S <- M S + S~
+        assert rel(host(M[h]) @ X + host(St[h]), rM @ X + rSt) < TOL_S
+        # M itself: relative, or, once it has decayed below 2^-14 of |S0| = |I|,
+        # relative to that (the scan's fp16 record operands hold terms down to
+        # 2^-24 of their own scale; one head here decays to |M| ~ 1e-27)
+        err = np.linalg.norm(host(M[h]) - rM)
+        assert err <= TOL_S * max(np.linalg.norm(rM), 2.0 ** -14 * np.sqrt(128)), err
 
 
 @pytest.mark.parametrize("n", [128, 256, 40])
