@@ -871,11 +871,15 @@ struct ScanCfg {
     static constexpr int OFF_SOP = 2 * AW_TILE;              // S operand [e][d]
     static constexpr int OFF_VOP = OFF_SOP + NE * D * 2;     // V' operand [e][t]
     static constexpr int G_TILE = C * NE * 2;                // g_in tile, [C][NE] bf16
-    static constexpr int OFF_G = OFF_VOP + NE * C * 2;
+    static constexpr int OFF_G = OFF_VOP + NE * C * 2;       // two g_in tiles, one per chunk parity
     static constexpr int KT_BYTES = 128 * C * 2;             // (K gamma_C / Gamma)^T [128 rows][C]
-    static constexpr int OFF_K0 = OFF_G + G_TILE;            // MMA 3's A operand, one buffer per chunk parity
+    static constexpr int OFF_K0 = OFF_G + 2 * G_TILE;        // MMA 3's A operand, one buffer per chunk parity
     static constexpr int OFF_K1 = OFF_K0 + KT_BYTES;
-    static constexpr int OFF_SMALL = OFF_K1 + KT_BYTES;
+    static constexpr int GFS = NE + 4;                       // row stride (floats) of a gate-factor tile
+    static constexpr int GF_TILE = C * GFS * 4;              // w Sigmoid(g_in) of the output rows, [C][GFS] fp32
+    static constexpr int OFF_GF0 = OFF_K1 + KT_BYTES;        // one tile per chunk parity
+    static constexpr int OFF_GF1 = OFF_GF0 + GF_TILE;
+    static constexpr int OFF_SMALL = OFF_GF1 + GF_TILE;
     // small region (floats): peers' row sums of squares [2 parity][R source][C], this
     // CTA's half-row sums [2 parity][2 half][C], RMSNorm weights of this CTA's columns
     // [NE], the columns' scale factors 2^-c and 2^c [NE each], the columns' largest
@@ -983,13 +987,14 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint64_t* bar_m2 = bars;             // MMA 2 of chunk j done (phase j)
     uint64_t* bar_m3 = bars + 1;         // MMA 3 of chunk j done (phase j)
     uint64_t* bar_aw = bars + 2;         // [2] A tile of chunk j landed in buffer j & 1
-    uint64_t* bar_g = bars + 4;          // g_in tile of chunk j landed (phase j)
-    uint64_t* bar_gfree = bars + 5;      // the output warps have read the g_in tile of chunk j
+
     uint64_t* bar_full = bars + 6;       // [2] peers' row sums of chunk j landed in s_rowsq[j & 1]
     uint64_t* bar_k = bars + 8;          // [2] (K gamma_C / Gamma)^T of chunk j landed in buffer j & 1
     uint64_t* bar_awfree = bar_k + 2;    // [2] MMA 2 has read A-tile buffer b (one phase per use)
     uint64_t* bar_kfree = bar_awfree + 2;   // [2] MMA 3 has read K buffer b (one phase per use)
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_kfree + 2);
+    uint64_t* bar_g = bar_kfree + 2;     // [2] g_in tile of chunk j landed in buffer j & 1 (one phase per use)
+    uint64_t* bar_gfree = bar_g + 2;     // [2] the V' warps have read g_in buffer b (one phase per use)
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_gfree + 2);
 
     const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
@@ -1010,7 +1015,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     auto rec_of = [&](int j) { return (long)(g0 + j) * H + h; };
     auto aw_buf = [&](int b) { return sm + (b ? Cfg::OFF_AW1 : Cfg::OFF_AW0); };
     auto k_buf = [&](int b) { return sm + (b ? Cfg::OFF_K1 : Cfg::OFF_K0); };
-    uint8_t* sG = sm + Cfg::OFF_G;
+    auto g_buf = [&](int b) { return sm + Cfg::OFF_G + b * Cfg::G_TILE; };
+    auto gf_buf = [&](int b) { return reinterpret_cast<float*>(sm + (b ? Cfg::OFF_GF1 : Cfg::OFF_GF0)); };
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
     const int vmx = (tid < NE && !w.zero_v) ? w.vmax[((size_t)n * H + h) * D + NE * r + tid] : 0;
@@ -1021,14 +1027,15 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     if (tid == 0) {
         tc::mbar_init(bar_m2, 1);
         tc::mbar_init(bar_m3, 1);
-        tc::mbar_init(bar_g, 1);
-        tc::mbar_init(bar_gfree, 4);                  // one arrival per output warp
+
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(bar_aw + b, 1);
             tc::mbar_init(bar_full + b, 1);
             tc::mbar_init(bar_k + b, 1);
             tc::mbar_init(bar_awfree + b, 1);
             tc::mbar_init(bar_kfree + b, 1);
+            tc::mbar_init(bar_g + b, 1);
+            tc::mbar_init(bar_gfree + b, 4);          // one arrival per V' warp
         }
         tc::mbar_fence_init();
     }
@@ -1076,7 +1083,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             if (++i == tc::WAIT_POLLS) xdead = true;
     };
     // phases each issuing lane armed or issued on each mbarrier, for the drain
-    uint32_t n_aw[2] = {0, 0}, n_k[2] = {0, 0}, n_full[2] = {0, 0}, n_g = 0;
+    uint32_t n_aw[2] = {0, 0}, n_k[2] = {0, 0}, n_full[2] = {0, 0}, n_g[2] = {0, 0};
     uint32_t n_m2 = 0, n_m3 = 0, n_awf[2] = {0, 0}, n_kf[2] = {0, 0};
 
     if (warp == Cfg::WARP_LOAD) {
@@ -1092,10 +1099,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int s = 0; s < 2; ++s)   // two 64-column slabs
                     tc::tma_load_2d(aw_buf(b) + s * (Cfg::AW_TILE / 2), &tm_aw, 64 * s, (int)(rec_of(j) * 128), bar_aw + b);
             };
-            auto load_g = [&](int j) {
-                ++n_g;
-                tc::mbar_arrive_expect_tx(bar_g, Cfg::G_TILE);
-                tc::tma_load_2d(sG, &tm_g, h * D + NE * r, t_begin + C * j, bar_g);
+            auto load_g = [&](int j) {   // into buffer j & 1
+                const int b = j & 1;
+                ++n_g[b];
+                tc::mbar_arrive_expect_tx(bar_g + b, Cfg::G_TILE);
+                tc::tma_load_2d(g_buf(b), &tm_g, h * D + NE * r, t_begin + C * j, bar_g + b);
             };
             auto load_k = [&](int j) {   // chunk j's K^T: one 64-token slab
                 const int b = j & 1;
@@ -1104,7 +1112,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::tma_load_2d(k_buf(b), &tm_kt, 0, (int)(rec_of(j) * 128), bar_k + b);
             };
             for (int j = 0; j < 2 && j < nch; ++j) { load_aw(j); load_k(j); }
-            if (gate && nch > 0) load_g(0);
+            for (int j = 0; gate && j < 2 && j < nch; ++j) load_g(j);
             for (int j = 0; j < nch && !timed_out; ++j) {
                 // buffers j & 1 of chunk j + 2 once MMA 2 / MMA 3 of chunk j have read them
                 // (barriers of those buffers' own: their next phases need these very loads,
@@ -1112,7 +1120,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 if (j + 2 < nch) { wait(bar_awfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_aw(j + 2); }
                 if (j + 2 < nch) { wait(bar_kfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_k(j + 2); }
                 // the g_in tile of chunk j + 1 once the outputs of chunk j are written
-                if (gate && j + 1 < nch) { wait(bar_gfree, j & 1); if (!timed_out) load_g(j + 1); }
+                // the g_in tile of chunk j + 2 once the V' warps have read chunk j's
+                if (gate && j + 2 < nch) { wait(bar_gfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_g(j + 2); }
             }
         }
         __syncwarp();
@@ -1217,7 +1226,6 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 }
             }
             if (gate) {
-                wait(bar_g, jo & 1);
                 wait_cl(bar_full + bo, (jo >> 1) & 1);
                 if (t < nco) {
                     float tot = s_rowpart[(bo * 2) * C + t] + s_rowpart[(bo * 2 + 1) * C + t];
@@ -1226,19 +1234,15 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                         if (p != r) tot += s_rowsq[(bo * R + p) * C + t];
                     const float rr = rsqrtf(tot * (1.0f / D) + a.norm_eps);
                     uint16_t* yp = reinterpret_cast<uint16_t*>(a.y) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
+                    const float* gf = gf_buf(bo) + t * Cfg::GFS + c_lo;   // w Sigmoid(g_in), by the V' warps
 #pragma unroll
                     for (int c = 0; c < HW; c += 8) {
-                        const uint4 g8 = *reinterpret_cast<const uint4*>(sG + gtile_offset<NE>(t, c_lo + c));
-                        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
-                        const float4 wa = reinterpret_cast<const float4*>(s_normw + c_lo + c)[0];
-                        const float4 wb = reinterpret_cast<const float4*>(s_normw + c_lo + c)[1];
-                        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+                        const float4 fa = reinterpret_cast<const float4*>(gf + c)[0];
+                        const float4 fb = reinterpret_cast<const float4*>(gf + c)[1];
+                        const float fv[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
                         float yv[8];
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
-                            yv[jj] = __fdividef(o[c + jj] * wv[jj] * rr, 1.0f + __expf(-gv));
-                        }
+                        for (int jj = 0; jj < 8; ++jj) yv[jj] = o[c + jj] * rr * fv[jj];
                         store8_bf16(yp + c, yv);
                     }
                 }
@@ -1282,14 +1286,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             //      refilled next), the next record into the other TMEM buffer, the one
             //      after it into registers
             if (!vrow) {
-                if (j > 0 && (a.o || gate)) {
-                    emit_outputs(j - 1, x_prev);
-                    if (gate) {
-                        // the g_in tile of chunk j - 1 is read
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_local(bar_gfree);
-                    }
-                }
+                if (j > 0 && (a.o || gate)) emit_outputs(j - 1, x_prev);
                 // arm this chunk's exchange barrier (its phase for chunk j - 2 completed:
                 // this thread waited for it in emit_outputs; a peer that stopped leaves
                 // it open, and then it is not armed again)
@@ -1300,7 +1297,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             }
             if (j + 1 < nch) { store_rec(j + 1); gm_next = gm_of(j + 1); }
             if (j + 3 < nch) load_rec(j + 3);   // into the set just stored from
-            tc::tmem_st_wait();
+            // (the U rows' TMEM stores complete before this chunk's state barrier, where
+            // the state update waits for all of this thread's TMEM stores)
             wait(bar_m2, j & 1);
             tc::fence_after_sync();
 
@@ -1423,6 +1421,30 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
             }
+            // ---- V' rows, off the recurrence path: w Sigmoid(g_in) of output row t =
+            //      row of this chunk (this thread's columns), read by the output thread
+            //      of the same row and columns in the next chunk
+            if (gate && vrow) {
+                wait(bar_g + b, (j >> 1) & 1);
+                const int t = row;
+                const uint8_t* sg = g_buf(b);
+                float* gf = gf_buf(b) + t * Cfg::GFS + c_lo;
+#pragma unroll
+                for (int c = 0; c < HW; c += 8) {
+                    const uint4 g8 = *reinterpret_cast<const uint4*>(sg + gtile_offset<NE>(t, c_lo + c));
+                    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+                    float fv[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const float gv = __uint_as_float((jj & 1) ? (gw[jj >> 1] & 0xffff0000u) : (gw[jj >> 1] << 16));
+                        fv[jj] = __fdividef(s_normw[c_lo + c + jj], 1.0f + __expf(-gv));
+                    }
+                    reinterpret_cast<float4*>(gf + c)[0] = make_float4(fv[0], fv[1], fv[2], fv[3]);
+                    reinterpret_cast<float4*>(gf + c)[1] = make_float4(fv[4], fv[5], fv[6], fv[7]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(bar_gfree + b);
+            }
             nbar_sync(NB_S, NS);
             x_prev = x_cur;
             x_cur = x_next;
@@ -1464,7 +1486,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                       tc::drain_phase(bar_awfree, n_awf[0]) & tc::drain_phase(bar_awfree + 1, n_awf[1]) &
                       tc::drain_phase(bar_kfree, n_kf[0]) & tc::drain_phase(bar_kfree + 1, n_kf[1]);
         if (warp == Cfg::WARP_LOAD && lane == 0) {
-            drained = tc::drain_phase(bar_g, n_g);
+            drained = tc::drain_phase(bar_g, n_g[0]) & tc::drain_phase(bar_g + 1, n_g[1]);
 #pragma unroll
             for (int b = 0; b < 2; ++b)
                 drained = drained & tc::drain_phase(bar_aw + b, n_aw[b]) & tc::drain_phase(bar_k + b, n_k[b]);
