@@ -84,6 +84,10 @@ TC_DEV uint32_t sw128_bf16(int row, int col) {
     return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 TC_DEV float4 ld_f4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+// byte offset of fp32 element (row, col) in a [rows][32] tile written by TMA with the 128-B swizzle
+TC_DEV uint32_t sw128_f32(int row, int col) {
+    return (uint32_t)(row * 128 + ((((col >> 2) ^ (row & 7))) << 4) + ((col & 3) << 2));
+}
 // 2^e as a float, e in [-126, 127]
 TC_DEV float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 // 16 values as fp16 in one 32-byte streaming store (p 32-byte aligned)
@@ -879,7 +883,13 @@ struct ScanCfg {
     static constexpr int GF_TILE = C * GFS * 4;              // w Sigmoid(g_in) of the output rows, [C][GFS] fp32
     static constexpr int OFF_GF0 = OFF_K1 + KT_BYTES;        // one tile per chunk parity
     static constexpr int OFF_GF1 = OFF_GF0 + GF_TILE;
-    static constexpr int OFF_SMALL = OFF_GF1 + GF_TILE;
+    // [U ; U_o] rows of a chunk (the CTA's NE columns, SW128 fp32 [128 rows][NE]) and
+    // gamma_C (128 floats) by TMA into a ring of NU buffers, loaded two chunks ahead
+    static constexpr int NU = 3;
+    static constexpr int U_TILE = 128 * NE * 4;
+    static constexpr int U_BUF = U_TILE + 128 * 4;
+    static constexpr int OFF_U = (OFF_GF1 + GF_TILE + 1023) / 1024 * 1024;
+    static constexpr int OFF_SMALL = OFF_U + NU * ((U_BUF + 1023) / 1024 * 1024);
     // small region (floats): peers' row sums of squares [2 parity][R source][C], this
     // CTA's half-row sums [2 parity][2 half][C], RMSNorm weights of this CTA's columns
     // [NE], the columns' scale factors 2^-c and 2^c [NE each], the columns' largest
@@ -949,7 +959,8 @@ TC_DEV uint32_t gtile_offset(int row, int col) {
 template <int R, bool TRANS>
 __global__ void __cluster_dims__(R, 1, 1) __launch_bounds__(ScanCfg<R>::NTS, 1)
 scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_aw,
-            const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_kt) {
+            const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_kt,
+            const __grid_constant__ CUtensorMap tm_uu) {
     using Cfg = ScanCfg<R>;
     constexpr int NE = Cfg::NE;
     constexpr int HW = NE / 2;           // value columns per epilogue thread
@@ -994,7 +1005,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     uint64_t* bar_kfree = bar_awfree + 2;   // [2] MMA 3 has read K buffer b (one phase per use)
     uint64_t* bar_g = bar_kfree + 2;     // [2] g_in tile of chunk j landed in buffer j & 1 (one phase per use)
     uint64_t* bar_gfree = bar_g + 2;     // [2] the V' warps have read g_in buffer b (one phase per use)
-    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_gfree + 2);
+    uint64_t* bar_u = bar_gfree + 2;     // [NU] U rows and gamma_C of chunk j landed in buffer j % NU
+    uint64_t* bar_ufree = bar_u + Cfg::NU;   // [NU] the state warps have read buffer k (one phase per use)
+    uint32_t* tbase_ptr = reinterpret_cast<uint32_t*>(bar_ufree + Cfg::NU);
 
     const int r = blockIdx.x;            // value-column block == cluster rank
     const int h = blockIdx.y;
@@ -1016,6 +1029,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     auto aw_buf = [&](int b) { return sm + (b ? Cfg::OFF_AW1 : Cfg::OFF_AW0); };
     auto k_buf = [&](int b) { return sm + (b ? Cfg::OFF_K1 : Cfg::OFF_K0); };
     auto g_buf = [&](int b) { return sm + Cfg::OFF_G + b * Cfg::G_TILE; };
+    auto u_buf = [&](int k) { return sm + Cfg::OFF_U + k * ((Cfg::U_BUF + 1023) / 1024 * 1024); };
     auto gf_buf = [&](int b) { return reinterpret_cast<float*>(sm + (b ? Cfg::OFF_GF1 : Cfg::OFF_GF0)); };
 
     if (warp == 0) { tc::tmem_alloc(tbase_ptr, Cfg::TM_COLS); tc::tmem_relinquish(); }
@@ -1026,6 +1040,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     }
     if (tid == 0) {
         tc::mbar_init(bar_m2, 1);
+        for (int k = 0; k < Cfg::NU; ++k) {
+            tc::mbar_init(bar_u + k, 1);
+            tc::mbar_init(bar_ufree + k, 8);          // one arrival per epilogue warp
+        }
         tc::mbar_init(bar_m3, 1);
 
         for (int b = 0; b < 2; ++b) {
@@ -1083,7 +1101,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             if (++i == tc::WAIT_POLLS) xdead = true;
     };
     // phases each issuing lane armed or issued on each mbarrier, for the drain
-    uint32_t n_aw[2] = {0, 0}, n_k[2] = {0, 0}, n_full[2] = {0, 0}, n_g[2] = {0, 0};
+    uint32_t n_aw[2] = {0, 0}, n_k[2] = {0, 0}, n_full[2] = {0, 0}, n_g[2] = {0, 0}, n_u[Cfg::NU] = {};
     uint32_t n_m2 = 0, n_m3 = 0, n_awf[2] = {0, 0}, n_kf[2] = {0, 0};
 
     if (warp == Cfg::WARP_LOAD) {
@@ -1091,6 +1109,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         if (lane == 0) {
             tc::tma_prefetch_desc(&tm_aw);
             tc::tma_prefetch_desc(&tm_kt);
+            tc::tma_prefetch_desc(&tm_uu);
             if (gate) tc::tma_prefetch_desc(&tm_g);
             auto load_aw = [&](int j) {
                 const int b = j & 1;
@@ -1111,6 +1130,14 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 tc::mbar_arrive_expect_tx(bar_k + b, Cfg::KT_BYTES);
                 tc::tma_load_2d(k_buf(b), &tm_kt, 0, (int)(rec_of(j) * 128), bar_k + b);
             };
+            auto load_u = [&](int j) {   // chunk j's U rows (this CTA's columns) and gamma_C
+                const int k = j % Cfg::NU;
+                ++n_u[k];
+                tc::mbar_arrive_expect_tx(bar_u + k, (w.zero_v ? 0 : Cfg::U_TILE) + 128 * 4);
+                if (!w.zero_v) tc::tma_load_2d(u_buf(k), &tm_uu, NE * r, (int)(rec_of(j) * 128), bar_u + k);
+                tc::bulk_load(u_buf(k) + Cfg::U_TILE, w.gm + rec_of(j) * GM_FLOATS, 128 * 4, bar_u + k);
+            };
+            for (int j = 0; j < Cfg::NU && j < nch; ++j) load_u(j);
             for (int j = 0; j < 2 && j < nch; ++j) { load_aw(j); load_k(j); }
             for (int j = 0; gate && j < 2 && j < nch; ++j) load_g(j);
             for (int j = 0; j < nch && !timed_out; ++j) {
@@ -1122,6 +1149,11 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 // the g_in tile of chunk j + 1 once the outputs of chunk j are written
                 // the g_in tile of chunk j + 2 once the V' warps have read chunk j's
                 if (gate && j + 2 < nch) { wait(bar_gfree + (j & 1), (j >> 1) & 1); if (!timed_out) load_g(j + 2); }
+                // chunk j + NU's U rows once the state warps have read chunk j's (in chunk j - 1)
+                if (j + Cfg::NU < nch) {
+                    wait(bar_ufree + j % Cfg::NU, (j / Cfg::NU) & 1);
+                    if (!timed_out) load_u(j + Cfg::NU);
+                }
             }
         }
         __syncwarp();
@@ -1169,38 +1201,33 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         nbar_sync(NB_S, NS);       // the epilogue's last arrival
     } else {
         // ------------------------------------------------------------------ epilogue
-        // record loads into registers: [U ; U_o] row `row`, this thread's HW of the
-        // CTA's columns, and gamma_C[row]
-        // Two register sets by chunk parity: the rows of chunk c are loaded in chunk
-        // c - 3 and stored into TMEM in chunk c - 1, so a load has two chunks to come
-        // back from DRAM (one chunk is close to the loaded DRAM's latency)
-        float pu0[HW], pu1[HW], pg0 = 0.f, pg1 = 0.f;
-        auto load_rec_to = [&](int j, float (&pu)[HW], float& pg) {
-            const float* u = w.uu + rec_of(j) * UU_FLOATS + (size_t)row * D + NE * r + c_lo;
-            if (!w.zero_v) {
-#pragma unroll
-                for (int i = 0; i < HW / 8; ++i) ld_nc_f8(u + 8 * i, pu + 8 * i);
-            }
-            pg = __ldg(w.gm + rec_of(j) * GM_FLOATS + row);
-        };
-        auto load_rec = [&](int j) {   // into the set of chunk j's parity
-            if (j & 1) load_rec_to(j, pu1, pg1); else load_rec_to(j, pu0, pg0);
-        };
-        auto store_from = [&](int b, const float (&pu)[HW]) {   // scaled by 2^-c (x = 0 with U)
+        // chunk j's record rows from U-ring buffer j % NU into TMEM buffer j & 1
+        // ([U ; U_o] row `row`, this thread's HW columns, scaled by 2^-c); returns
+        // gamma_C[row] of the chunk
+        auto store_rec = [&](int j) -> float {
+            const int k = j % Cfg::NU;
+            wait(bar_u + k, (j / Cfg::NU) & 1);
+            const uint8_t* ub = u_buf(k);
             if (!w.zero_v) {
 #pragma unroll
                 for (int i = 0; i < HW; i += 16) {
                     float v[16];
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = pu[i + k] * s_vsc[c_lo + i + k];
-                    tc::tmem_st16(T0 + Cfg::TM_D + NE * b + lane_base + c_lo + i, v);
+                    for (int q = 0; q < 16; q += 4) {
+                        const float4 u4 = *reinterpret_cast<const float4*>(ub + sw128_f32(row, c_lo + i + q));
+                        v[q] = u4.x * s_vsc[c_lo + i + q];
+                        v[q + 1] = u4.y * s_vsc[c_lo + i + q + 1];
+                        v[q + 2] = u4.z * s_vsc[c_lo + i + q + 2];
+                        v[q + 3] = u4.w * s_vsc[c_lo + i + q + 3];
+                    }
+                    tc::tmem_st16(T0 + Cfg::TM_D + NE * (j & 1) + lane_base + c_lo + i, v);
                 }
             }
+            const float g = reinterpret_cast<const float*>(ub + Cfg::U_TILE)[row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(bar_ufree + k);
+            return g;
         };
-        auto store_rec = [&](int j) {  // chunk j's rows into TMEM buffer j & 1
-            if (j & 1) store_from(1, pu1); else store_from(0, pu0);
-        };
-        auto gm_of = [&](int j) { return (j & 1) ? pg1 : pg0; };
         // o and y of chunk jo from its TMEM buffer (output-row threads)
         auto emit_outputs = [&](int jo, int xo) {   // xo: the chunk's exponent
             const int bo = jo & 1;
@@ -1266,9 +1293,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int jj = 0; jj < 16; ++jj)
                     *reinterpret_cast<uint16_t*>(sSop + tc::sw128_offset_h(c + jj, d, NE)) = tc::f32_to_f16(v[jj]);
             }
-            if (nch > 0) { load_rec(0); store_rec(0); gm_next = gm_of(0); }
-            if (nch > 1) load_rec(1);
-            if (nch > 2) load_rec(2);
+            if (nch > 0) gm_next = store_rec(0);
             tc::tmem_st_wait();
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -1295,8 +1320,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                     else { ++n_full[b]; tc::mbar_arrive_expect_tx(bar_full + b, (R - 1) * C * 4); }
                 }
             }
-            if (j + 1 < nch) { store_rec(j + 1); gm_next = gm_of(j + 1); }
-            if (j + 3 < nch) load_rec(j + 3);   // into the set just stored from
+            if (j + 1 < nch) gm_next = store_rec(j + 1);
             // (the U rows' TMEM stores complete before this chunk's state barrier, where
             // the state update waits for all of this thread's TMEM stores)
             wait(bar_m2, j & 1);
@@ -1487,6 +1511,7 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                       tc::drain_phase(bar_kfree, n_kf[0]) & tc::drain_phase(bar_kfree + 1, n_kf[1]);
         if (warp == Cfg::WARP_LOAD && lane == 0) {
             drained = tc::drain_phase(bar_g, n_g[0]) & tc::drain_phase(bar_g + 1, n_g[1]);
+            for (int k = 0; k < Cfg::NU; ++k) drained = drained & tc::drain_phase(bar_u + k, n_u[k]);
 #pragma unroll
             for (int b = 0; b < 2; ++b)
                 drained = drained & tc::drain_phase(bar_aw + b, n_aw[b]) & tc::drain_phase(bar_k + b, n_k[b]);
@@ -1608,7 +1633,9 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
                       NE == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess) return e;
     if ((e = make_map(&maw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.aw, 128, (uint64_t)L.nrec * 128, 64, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
-    CUtensorMap mkt;
+    CUtensorMap mkt, muu;
+    if ((e = make_map(&muu, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.uu, 128, (uint64_t)L.nrec * 128, NE, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
     if ((e = make_map(&mkt, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, w.kt, spl::C, (uint64_t)L.nrec * 128, 64, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
 
@@ -1630,7 +1657,8 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
     if (parts & 2) {
         dim3 grid(spl::SCAN_R, a.H, a.num_seqs);
         auto kern = w.zero_v ? spl::scan_kernel<spl::SCAN_R, true> : spl::scan_kernel<spl::SCAN_R, false>;
-        kern<<<grid, spl::ScanCfg<spl::SCAN_R>::NTS, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt);
+        kern<<<grid, spl::ScanCfg<spl::SCAN_R>::NTS, spl::ScanCfg<spl::SCAN_R>::SMEM_BYTES, s>>>(a, w, maw, mg, mkt,
+                                                                                                   muu);
         ++launched;
     }
     count_launches(launched);

@@ -215,6 +215,13 @@ TC_DEV void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* mbar
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
         : "memory");
 }
+// untiled bulk copy global -> shared: dst, src 16-byte aligned, bytes a multiple of 16
+TC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(mbar))
+        : "memory");
+}
 TC_DEV void tma_prefetch_desc(const void* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
