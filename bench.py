@@ -310,7 +310,7 @@ def run_ours(args, rank, world):
         achieved = alg_bytes / (ms * 1e-3) / 1e9
         return {"metric": METRIC, "value": world * T / (ms_all * 1e-3), "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "tf32", "data": "synthetic (seeded)",
+                "scaling": "weak", "vs_baseline": None, "dtype": "tf32+fp16", "data": "synthetic (seeded)",
                 "config": {"workload": args.workload, "tokens": T, "num_seqs": N, "H": H, "dk": d, "dv": d},
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                              "frac": achieved / pk["hbm"], "algorithmic_bytes_per_launch": alg_bytes},
@@ -512,7 +512,7 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "tf32" if path_tc else "f32",
+        "dtype": "tf32+fp16" if path_tc else "f32",   # tf32 chunk precompute, fp16 recurrence operands, FP32 accumulate
         "data": "synthetic (seeded, generated on the device)",
         "config": {"workload": args.workload, "tokens": T, "num_seqs": N, "H": H, "dk": d, "dv": d,
                    "qkv": "bf16", "S0": wl["S0"], "fused_gate": wl["gate"], "qk_l2norm": True,
