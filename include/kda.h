@@ -188,8 +188,10 @@ kda_status kda_prefill(const kda_prefill_args* args, void* stream);
  *   workspace is only read, so any number of scans may follow one records
  *   call, each on any stream ordered after it.  flags: 0, or KDA_SCAN_ZERO_V:
  *   evaluate the operator with v = 0 (the records' U parts are not read; the
- *   outputs are those of kda_prefill with a zero v).  Other flags ->
- *   KDA_ERR_SHAPE.
+ *   outputs are those of kda_prefill with a zero v, not bit for bit: this
+ *   scan also follows the decaying state's magnitude chunk by chunk, so that
+ *   a transition matrix keeps its precision until it has decayed below about
+ *   2^-24 of |S0|).  Other flags -> KDA_ERR_SHAPE.
  */
 #define KDA_SCAN_ZERO_V 1
 kda_status kda_prefill_records(const kda_prefill_args* args, void* stream);
