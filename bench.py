@@ -486,7 +486,7 @@ def run_ours(args, rank, world):
         bo = nbytes(host_o) + nbytes(host_y) + nbytes(host_S)
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "call": ("kda.prefill_from_host (slabs of %d tokens, copies overlapped)" % E2E_SLAB) if pipelined
+               "call": ("kda_prefill_from_host (C ABI, host buffers; slabs of %d tokens, copies overlapped)" % E2E_SLAB) if pipelined
                        else "copies, kda_prefill, copies on one stream"}
 
     if rank != 0:

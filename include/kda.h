@@ -233,6 +233,38 @@ kda_status kda_prefill_scan(const kda_prefill_args* args, int flags, void* strea
 kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
 
 /*
+ * kda_prefill of one sequence whose inputs and outputs are in HOST memory, the
+ * copies overlapped with the compute.  (Library plumbing: the pages have no
+ * counterpart.)
+ *
+ * args as for kda_prefill with num_seqs = 1 and T_total tokens, except that q,
+ * k, v, z, beta, A, S0 (may be NULL), g_in (may be NULL), norm_w (may be NULL),
+ * o, y and S_T are HOST pointers (page-locked memory, e.g. cudaHostAlloc, for
+ * the copies to overlap; pageable memory works but serialises them);
+ * cu_seqlens, cu_seqlens_host, workspace and workspace_bytes are ignored;
+ * snapshots are not taken (S_snap must be NULL, else KDA_ERR_UNSUPPORTED).
+ * The sequence is cut into slabs of `slab` tokens (a positive multiple of 64,
+ * else KDA_ERR_SHAPE); slab i resumes from the state slab i - 1 left, exactly
+ * as one kda_prefill call over the whole sequence would up to the power-of-two
+ * scales each slab's scan picks for its fp16 operands (equal to about 1e-6
+ * relative).  Host-to-device copies run one slab ahead and device-to-host
+ * copies one slab behind, on two streams the library creates for the call;
+ * the compute runs on `stream`, which on return is ordered after every copy:
+ * synchronise it before reading o, y, S_T or reusing the inputs.
+ *
+ * staging: caller-owned device memory of
+ * kda_prefill_from_host_staging_size(args, slab) bytes (16-byte aligned, else
+ * KDA_ERR_ALIGN; smaller -> KDA_ERR_WORKSPACE): double-buffered slab inputs and
+ * outputs, the carried state, and one slab's prefill workspace (the
+ * chunk-parallel schedule).  The staging is in use until `stream` completes.
+ * Errors: those of kda_prefill for the slab calls, KDA_ERR_CUDA for a failed
+ * copy or stream operation.
+ */
+size_t kda_prefill_from_host_staging_size(const kda_prefill_args* args, int slab);
+kda_status kda_prefill_from_host(const kda_prefill_args* args, int slab, void* staging, size_t staging_bytes,
+                                 void* stream);
+
+/*
  * The same operator as kda_prefill, always evaluated by the per-token
  * recurrence on CUDA cores (one CTA per sequence and head, the state held in
  * registers).  Same arguments, layouts, validation and status codes as

@@ -36,6 +36,11 @@ static std::atomic<uint32_t> g_wait_limit{KDA_WAIT_LIMIT_DEFAULT};   // kda_debu
 namespace kda {
 // called by every launch wrapper once per kernel enqueued
 void count_launches(int n) { g_launches += (uint64_t)n; }
+// a failed CUDA runtime call outside this file: its status and the error string
+kda_status cuda_failure(cudaError_t e) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    return KDA_ERR_CUDA;
+}
 // poll bound of the prefill kernels' waits on local copies and MMAs
 uint32_t wait_limit() {
     const uint32_t v = g_wait_limit.load(std::memory_order_relaxed);

@@ -15,6 +15,7 @@ void count_launches(int n);
 // poll bound of the prefill kernels' waits on local copies and MMAs (api.cu;
 // kda_debug_set_wait_limit)
 uint32_t wait_limit();
+kda_status cuda_failure(cudaError_t e);   // records the CUDA error string, returns KDA_ERR_CUDA
 
 // Logistic function through the hardware exp2 / fast-divide path.
 KDA_DEV float sigmoidf_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }

@@ -27,7 +27,8 @@ EXPORTED = ["kda_prefill", "kda_prefill_recurrent", "kda_prefill_workspace_size"
             "kda_decode_step", "kda_gate_norm", "kda_status_str", "kda_last_error_string",
             "kda_version", "kda_launch_count", "kda_prefill_noalloc", "kda_prefill_snapshot_count",
             "kda_short_conv", "kda_short_conv_step", "kda_kcp_apply", "kda_prefill_records",
-            "kda_prefill_scan", "kda_get_last_device_error", "kda_debug_set_wait_limit"]
+            "kda_prefill_scan", "kda_get_last_device_error", "kda_debug_set_wait_limit",
+            "kda_prefill_from_host", "kda_prefill_from_host_staging_size"]
 
 _vp = ctypes.c_void_p
 
@@ -130,6 +131,10 @@ def load_library(path: str = LIB_PATH):
     lib.kda_get_last_device_error.argtypes = [_vp, _vp]
     lib.kda_get_last_device_error.restype = ctypes.c_int
     lib.kda_debug_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.kda_prefill_from_host.argtypes = [ctypes.POINTER(PrefillArgs), ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+    lib.kda_prefill_from_host.restype = ctypes.c_int
+    lib.kda_prefill_from_host_staging_size.argtypes = [ctypes.POINTER(PrefillArgs), ctypes.c_int]
+    lib.kda_prefill_from_host_staging_size.restype = ctypes.c_size_t
     lib.kda_debug_set_wait_limit.restype = ctypes.c_uint32
     _lib = lib
     return lib
@@ -246,98 +251,48 @@ def release_workspace_cache():
     _WS_CACHE.clear()
 
 
-def prefill_from_host(q, k, v, z, beta, A, S0=None, g_in=None, norm_w=None, out=None, slab=16384,
-                      g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, gate="bounded"):
-    """KDA prefill of one sequence held in (pinned) host memory, results back to
-    host memory, with the copies overlapped with the compute.
+_STAGING = {}                 # prefill_from_host: one staging buffer per device
 
-    The sequence is cut into slabs of `slab` tokens (a multiple of 64); slab i's
-    prefill resumes from the state slab i-1 left (S0 aliasing S_T on the device).
-    Host-to-device copies run one slab ahead on their own stream, device-to-host
-    copies one slab behind on another, through double-buffered device staging.
-    q, k, v, g_in [T, H, d] bf16, z [T, H, d] f32, beta [T, H], A [H], S0
-    [1, H, d, d] or None; out = (o, y, S_T) host tensors (y None without g_in).
-    Returns (o, S_T, y) on the host.
+
+def prefill_from_host(q, k, v, z, beta, A, S0=None, g_in=None, norm_w=None, out=None, slab=16384,
+                      g_min=-5.0, scale=1.0, qk_l2norm=True, norm_eps=1e-6, gate="bounded", stream=None):
+    """KDA prefill of one sequence held in (pinned) host memory, results back to
+    host memory, through ``kda_prefill_from_host``: the library cuts the sequence
+    into slabs of ``slab`` tokens (a multiple of 64) and overlaps the copies with
+    the compute.  q, k, v, g_in [T, H, d] bf16 (or f32), z [T, H, d] f32, beta
+    [T, H], A [H], S0 [1, H, d, d] or None, all host tensors; out = (o, y, S_T)
+    host tensors (y None without g_in), allocated pinned when None.  The device
+    staging comes from a per-device cache.  Returns (o, S_T, y) on the host
+    once the call's stream has completed.
     """
-    if slab % 64:
-        raise ValueError("slab must be a multiple of 64 tokens")
     T, H, d = q.shape
+    dv = v.shape[2]
     dev = torch.device("cuda", torch.cuda.current_device())
     gate_on = g_in is not None
     if out is None:
-        out = (torch.empty((T, H, d), dtype=q.dtype).pin_memory(),
-               torch.empty((T, H, d), dtype=torch.bfloat16).pin_memory() if gate_on else None,
-               torch.empty((1, H, d, d), dtype=torch.float32).pin_memory())
+        out = (torch.empty((T, H, dv), dtype=q.dtype).pin_memory(),
+               torch.empty((T, H, dv), dtype=torch.bfloat16).pin_memory() if gate_on else None,
+               torch.empty((1, H, d, dv), dtype=torch.float32).pin_memory())
     o_h, y_h, S_h = out
-    L = min(slab, T)
-    names = ["q", "k", "v", "z", "beta"] + (["g_in"] if gate_on else [])
-    src = dict(q=q, k=k, v=v, z=z, beta=beta, g_in=g_in)
-    bufs = [{n: torch.empty((L,) + tuple(src[n].shape[1:]), dtype=src[n].dtype, device=dev) for n in names}
-            for _ in range(2)]
-    obufs = [(torch.empty((L, H, d), dtype=q.dtype, device=dev),
-              torch.empty((L, H, d), dtype=torch.bfloat16, device=dev) if gate_on else None) for _ in range(2)]
-    A_d = A.to(dev, non_blocking=True)
-    w_d = norm_w.to(dev, non_blocking=True) if norm_w is not None else None
-    state = S0.to(dev) if S0 is not None else torch.zeros((1, H, d, d), dtype=torch.float32, device=dev)
-    n_slabs = (T + L - 1) // L
-    last = T - (n_slabs - 1) * L
-    cu_h = {L: torch.tensor([0, L], dtype=torch.int32), last: torch.tensor([0, last], dtype=torch.int32)}
-    cu_d = {n: t.to(dev) for n, t in cu_h.items()}
+    a = PrefillArgs()
+    a.num_seqs, a.T_total, a.H, a.dk, a.dv = 1, int(T), int(H), int(d), int(dv)
+    a.qkv_dtype = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("z", z), ("beta", beta), ("A", A), ("S0", S0),
+                    ("o", o_h), ("S_T", S_h), ("g_in", g_in), ("norm_w", norm_w), ("y", y_h)):
+        setattr(a, name, t.data_ptr() if t is not None else None)
+    a.g_min, a.scale, a.qk_l2norm, a.norm_eps = float(g_min), float(scale), int(bool(qk_l2norm)), float(norm_eps)
+    a.gate_mode = GATES[gate]
+    lib = load_library()
+    need = int(lib.kda_prefill_from_host_staging_size(ctypes.byref(a), int(slab)))
+    if need == 0:
+        raise ValueError("kda_prefill_from_host: unsupported slab or shape")
     key = (dev.type, dev.index)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    s_cmp = torch.cuda.current_stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(n_slabs)]
-    ev_cmp = [torch.cuda.Event() for _ in range(n_slabs)]
-    ev_out = [torch.cuda.Event() for _ in range(n_slabs)]
-    start = torch.cuda.Event()
-    start.record(s_cmp)
-    s_in.wait_event(start)
-    s_out.wait_event(start)
-
-    def upload(i):
-        b = i & 1
-        t0, t1 = i * L, min(T, (i + 1) * L)
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev_cmp[i - 2])          # slab i-2 has consumed this buffer
-            for n in names:
-                bufs[b][n][: t1 - t0].copy_(src[n][t0:t1], non_blocking=True)
-            ev_in[i].record(s_in)
-
-    upload(0)
-    for i in range(n_slabs):
-        if i + 1 < n_slabs:
-            upload(i + 1)
-        b = i & 1
-        t0, t1 = i * L, min(T, (i + 1) * L)
-        n_tok = t1 - t0
-        s_cmp.wait_event(ev_in[i])
-        if i >= 2:
-            s_cmp.wait_event(ev_out[i - 2])             # outputs of slab i-2 are on the host
-        ob, yb = obufs[b]
-        bb = bufs[b]
-        sl = slice(0, n_tok)
-        args = make_prefill_args(bb["q"][sl], bb["k"][sl], bb["v"][sl], bb["z"][sl], bb["beta"][sl], A_d,
-                                 cu_d[n_tok], cu_h[n_tok], ob[sl], S0=state, S_T=state,
-                                 g_in=bb["g_in"][sl] if gate_on else None, norm_w=w_d,
-                                 y=yb[sl] if gate_on else None, g_min=g_min, scale=scale, qk_l2norm=qk_l2norm,
-                                 norm_eps=norm_eps, gate=gate)
-        need = prefill_workspace_size(args)
-        ws = _WS_CACHE.get(key)
-        if ws is None or ws.numel() < need:
-            _WS_CACHE[key] = ws = torch.empty(need, dtype=torch.uint8, device=dev)
-        args.workspace, args.workspace_bytes = ws.data_ptr(), ws.numel()
-        prefill_raw(args, stream=s_cmp)
-        ev_cmp[i].record(s_cmp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_cmp[i])
-            o_h[t0:t1].copy_(ob[sl], non_blocking=True)
-            if gate_on:
-                y_h[t0:t1].copy_(yb[sl], non_blocking=True)
-            if i == n_slabs - 1:
-                S_h.copy_(state, non_blocking=True)
-            ev_out[i].record(s_out)
-    s_cmp.wait_event(ev_out[n_slabs - 1])
+    st = _STAGING.get(key)
+    if st is None or st.numel() < need:
+        _STAGING[key] = st = torch.empty(need, dtype=torch.uint8, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    _check(lib.kda_prefill_from_host(ctypes.byref(a), int(slab), st.data_ptr(), st.numel(), _stream(s)),
+           "kda_prefill_from_host")
     return o_h, S_h, y_h
 
 

@@ -195,3 +195,25 @@ def test_records_and_scan_validation(kda_lib):
     f, _c2 = _args(kda, qkv_dtype=kda.KDA_F32, workspace=FAKE, workspace_bytes=1 << 40)
     assert kda_lib.kda_prefill_records(ctypes.byref(f), None) == 6         # no chunk-parallel schedule
     assert kda_lib.kda_prefill_scan(ctypes.byref(f), kda.SCAN_ZERO_V, None) == 6
+
+
+def test_prefill_from_host_validation(kda_lib):
+    """kda_prefill_from_host: one sequence, slabs a positive multiple of 64, no
+    snapshots, host inputs and outputs present, caller staging of the size
+    kda_prefill_from_host_staging_size gives (checked before anything is
+    enqueued)."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    a, _cu = _args(kda, T_total=1000, S_T=FAKE)
+    need = kda_lib.kda_prefill_from_host_staging_size(ctypes.byref(a), 256)
+    assert need > 2 * 256 * 2 * 128 * (3 * 2 + 4)            # two slabs of q, k, v (bf16) and z at least
+    assert kda_lib.kda_prefill_from_host_staging_size(ctypes.byref(a), 100) == 0
+    bigger = kda_lib.kda_prefill_from_host_staging_size(ctypes.byref(a), 512)
+    assert bigger > need
+    call = lambda b, slab=256, st=FAKE, n=need: kda_lib.kda_prefill_from_host(ctypes.byref(b), slab, st, n, None)
+    assert call(a, slab=0) == 2 and call(a, slab=100) == 2
+    assert call(_args(kda, T_total=1000, S_T=FAKE, num_seqs=2)[0]) == 2
+    assert call(_args(kda, T_total=1000, S_T=FAKE, S_snap=FAKE, snap_interval=64)[0]) == 6
+    assert call(_args(kda, T_total=1000, S_T=FAKE, q=None)[0]) == 1
+    assert call(_args(kda, T_total=1000)[0]) == 1                   # no S_T
+    assert call(_args(kda, T_total=1000, S_T=FAKE, g_in=FAKE)[0]) == 1   # g_in without y
+    assert call(a, st=None) == 8 and call(a, st=FAKE + 8) == 4 and call(a, n=need - 1) == 8
