@@ -37,7 +37,7 @@ TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense tf32 : bf16 ratio (GB300)
 SNAP_INTERVAL = 1024            # prefix-cache block: one state snapshot per 1024 tokens
 PROLOGUE_WIDTH = 4              # ShortConv width (not given by the KDA pages; a parameter)
 KCP_RANKS = 8                   # context-parallel split measured by the KCP secondary
-E2E_SLAB = 16384                # tokens per slab of the pipelined host-buffer prefill
+E2E_SLAB = 4096     # slab of the host-buffer pipeline (measured: 4096 34.2 ms, 16384 35.5 ms per 128k step)
 
 WORKLOADS = {
     "prefill_128k": dict(T=131072, H=32, d=128, S0=True, gate=True, varlen=None),
