@@ -133,6 +133,9 @@ def test_records_then_scans_equal_prefill(kda_lib, cuda_dev):
     _, Sz, _ = kda.prefill_scan(rec, want_o=False)                       # from zero, records reused
     _, Sz1, _ = kda.prefill(q, k, v, z, beta, A, cu_seqlens=cu_d, want_o=False)
     assert torch.equal(Sz, Sz1)
+    # bit for bit here: over these 700 tokens the largest |S| stays within [2^-6, 2^6]
+    # of its starting scale, so the zero-v (transition) scan never moves its
+    # state exponent and computes exactly what the plain scan does
     o3, S3, _ = kda.prefill_scan(rec, S0=S0, zero_v=True)
     o4, S4, _ = kda.prefill(q, k, torch.zeros_like(v), z, beta, A, cu_seqlens=cu_d, S0=S0)
     torch.cuda.synchronize()
