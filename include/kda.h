@@ -243,6 +243,7 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, void* stream);
  * the copies to overlap; pageable memory works but serialises them);
  * cu_seqlens, cu_seqlens_host, workspace and workspace_bytes are ignored;
  * snapshots are not taken (S_snap must be NULL, else KDA_ERR_UNSUPPORTED).
+ * With T_total = 0 the token arrays may be NULL and S_T receives S0 (or 0).
  * The sequence is cut into slabs of `slab` tokens (a positive multiple of 64,
  * else KDA_ERR_SHAPE); slab i resumes from the state slab i - 1 left, exactly
  * as one kda_prefill call over the whole sequence would up to the power-of-two

@@ -91,7 +91,8 @@ kda_status kda_prefill_from_host(const kda_prefill_args* a, int slab, void* stag
     if (slab <= 0 || slab % 64 || a->num_seqs != 1 || a->T_total < 0 || a->H <= 0 || a->dk <= 0 || a->dv <= 0)
         return KDA_ERR_SHAPE;
     if (a->S_snap) return KDA_ERR_UNSUPPORTED;
-    if (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->A || !a->o || !a->S_T) return KDA_ERR_NULL;
+    if (!a->A || !a->S_T) return KDA_ERR_NULL;
+    if (a->T_total > 0 && (!a->q || !a->k || !a->v || !a->z || !a->beta || !a->o)) return KDA_ERR_NULL;
     if (a->g_in && !a->y) return KDA_ERR_NULL;
     if (!staging) return KDA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(staging) & 15u) return KDA_ERR_ALIGN;

@@ -354,3 +354,44 @@ def test_fp16_operand_range(kda_lib, cuda_dev, case):
         parity("S_T / column scale", host(S_T) / col, rS / col, TOL_S)
     if ry is not None:
         parity("y", host(y), ry, TOL_O, bf16_out=True, floor_ref=ro)
+
+
+def test_prefill_from_host_edge_cases(kda_lib, cuda_dev):
+    """kda_prefill_from_host on an empty sequence (S_T = S0, nothing else
+    written), on float32 q/k/v with d = 64 in slabs of 64 tokens (a ragged last
+    slab), and with a slab longer than the sequence; against kda_prefill on the
+    device and the oracle."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    # empty sequence: the state passes through
+    d = I.make_prefill(I.workload("tiny", T=0, H=2, dk=64, dv=64, S0_std=0.02))
+    S0 = (0.02 * np.random.default_rng(3).standard_normal((1, 2, 64, 64))).astype(np.float32)
+    empty = lambda shape: torch.empty(shape, dtype=torch.float32).pin_memory()
+    o_h, S_h, _ = kda.prefill_from_host(empty((0, 2, 64)), empty((0, 2, 64)), empty((0, 2, 64)), empty((0, 2, 64)),
+                                        empty((0, 2)), pin(d["A"]), S0=pin(S0), slab=64)
+    torch.cuda.synchronize()
+    assert np.array_equal(S_h.numpy(), S0)
+    # float32, d = 64, 130 tokens in slabs of 64 and in one slab of 4096
+    d = I.make_prefill(I.workload("tiny", T=130, H=2, dk=64, dv=64, S0_std=0.02, z_std=2.0, A_std=0.5))
+    S0 = (0.02 * np.random.default_rng(4).standard_normal((1, 2, 64, 64))).astype(np.float32)
+    ro, rS, _ = oracle.prefill(f64(d, "q"), f64(d, "k"), f64(d, "v"), d["z"], d["beta"], d["A"], S0=S0)
+    q, k, v = qkv_to_dev(d, cuda_dev)
+    o_d, S_d, _ = kda.prefill(q, k, v, to_dev(d["z"], cuda_dev), to_dev(d["beta"], cuda_dev),
+                              to_dev(d["A"], cuda_dev), S0=to_dev(S0, cuda_dev))
+    for slab in (64, 4096):
+        o_h, S_h, _ = kda.prefill_from_host(pin(d["q"]), pin(d["k"]), pin(d["v"]), pin(d["z"]), pin(d["beta"]),
+                                            pin(d["A"]), S0=pin(S0), slab=slab)
+        torch.cuda.synchronize()
+        parity(f"o slab {slab}", o_h.numpy(), ro, TOL_O)
+        parity(f"S_T slab {slab}", S_h.numpy(), rS, TOL_S)
+        parity(f"o slab {slab} vs device call", o_h.numpy(), host(o_d), 1e-4, row_tol=1e-2)
+    # bf16 with the fused gate, one slab longer than the sequence
+    d = I.make_prefill(I.workload("prefill_128k", T=100, H=2))
+    hp = lambda x, bf: (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16) if bf
+                        else torch.from_numpy(np.ascontiguousarray(x))).pin_memory()
+    o_h, S_h, y_h = kda.prefill_from_host(hp(d["q"], True), hp(d["k"], True), hp(d["v"], True), hp(d["z"], False),
+                                          hp(d["beta"], False), hp(d["A"], False), S0=hp(d["S0"], False),
+                                          g_in=hp(d["g_in"], True), slab=16384)
+    torch.cuda.synchronize()
+    ro, rS, ry = run_oracle(d)
+    check((o_h, S_h, y_h), (ro, rS, ry))
