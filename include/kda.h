@@ -99,7 +99,7 @@ typedef enum { KDA_GATE_BOUNDED = 0, KDA_GATE_SOFTPLUS = 1 } kda_gate;
  * schedule.  bf16, d = 128 (the tensor-core path):
  *  - workspace_bytes >= kda_prefill_workspace_size(): chunk-parallel schedule
  *    (one pass over all (chunk, head) pairs in parallel writes each chunk's
- *    state-free terms, 112.5 KiB per chunk and head, to the workspace; a second
+ *    state-free terms, 112.75 KiB per chunk and head, to the workspace; a second
  *    pass runs the state recurrence per (sequence, head) on fp16 tensor-core
  *    operands under exact power-of-two scaling).  The fastest.
  *  - KDA_PREFILL_MIN_WORKSPACE <= workspace_bytes < that: single-pass schedule

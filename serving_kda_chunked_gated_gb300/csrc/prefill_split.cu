@@ -53,7 +53,7 @@ constexpr int SCAN_R = 4; // scan: CTAs (value-column blocks) per (sequence, hea
 constexpr size_t AW_ELEMS = 128 * 128;    // [-W ; Gamma Q - P Gamma K]  [row][d]  fp16
 constexpr size_t UU_FLOATS = 128 * 128;   // [U ; U_o]                   [row][e]  FP32
 constexpr size_t KT_ELEMS = 128 * 64;     // (K gamma_C / Gamma)^T       [d][t]    fp16
-constexpr size_t GM_FLOATS = 128;         // gamma_C                     [d]       FP32
+constexpr size_t GM_FLOATS = 192;         // [gamma_C ; rho]             [d] [t]   FP32
 
 struct Work {
     const int* chunk_base;   // [num_seqs + 1] first global chunk of each sequence
@@ -374,7 +374,77 @@ prep_kernel(kda_prefill_args a, Work w,
     float beta_next = 0.f;
     if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
 
+    // The output rows (row >= C) of a record's A tile, Gamma Q - P Gamma K: 16 of the
+    // row's columns of this thread into v, from TMEM (P Gamma K) and shared memory (q~
+    // and the sub-chunk decays).
+    auto a_row = [&](int c, float* v) {
+        const int t = row - C;
+        const float* es = s_expS + ((t & (C - 1)) >> 4) * D;
+        tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const int d = 32 * grp + c + j;
+            const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
+            const float4 e4 = *reinterpret_cast<const float4*>(es + d);
+            v[j] = q4.x * e4.x - v[j];
+            v[j + 1] = q4.y * e4.y - v[j + 1];
+            v[j + 2] = q4.z * e4.z - v[j + 2];
+            v[j + 3] = q4.w * e4.w - v[j + 3];
+        }
+    };
+    // the four column groups' largest |A| and |U_o| of each output row, from phase 6 of
+    // a record to phase 1b of the next (the diagonal-block buffer is free in between)
+    float* s_rmax = s_diag;
+    // Output row t of record pr's A tile and of its U_o are stored times 2^s_t, and
+    // rho_t = 2^-s_t goes with gamma_C; the scan multiplies the row's sum back by rho_t.
+    // A row whose every decay factor is small would otherwise sit among the fp16
+    // subnormals and keep only a few bits, and times a large state its product with S
+    // is not small.  A row whose largest entry is below 2^-7 is raised to [1/2, 1) (by
+    // at most 2^96, and U_o's row stays below 2^120); the others keep s_t = 0, rho_t = 1
+    // (their entries below the fp16 normals are under 2^-7 of the row's largest).
+    // Phase 6 leaves the A rows in TMEM (in place of P Gamma K) beside U_o; this runs at
+    // the start of the next record, while the others compute the L2 norms, so that no
+    // barrier of its own is needed.
+    auto write_a_rows = [&](long pr) {
+        tc::fence_after_sync();
+        const int t = row - C;
+        const float ma = fmaxf(fmaxf(s_rmax[t], s_rmax[C + t]), fmaxf(s_rmax[2 * C + t], s_rmax[3 * C + t]));
+        const float* sm2 = s_rmax + 4 * C;
+        const float mu = fmaxf(fmaxf(sm2[t], sm2[C + t]), fmaxf(sm2[2 * C + t], sm2[3 * C + t]));
+        // m = f 2^e with f in [1/2, 1): e from the exponent bits (a subnormal ma reads
+        // as e = -126, beyond the cap); U_o's row stays below 2^120
+        const int eu = (mu > 0.f && mu <= 3.0e38f) ? (int)((__float_as_uint(mu) >> 23) & 0xffu) - 126 : 0;
+        const int st = (ma > 0.f && ma < 0.0078125f)
+                           ? max(0, min(min(96, 126 - (int)((__float_as_uint(ma) >> 23) & 0xffu)), 120 - eu))
+                           : 0;
+        const float up = __int_as_float((127 + st) << 23);
+        if (grp == 0) w.gm[pr * GM_FLOATS + D + t] = __int_as_float((127 - st) << 23);
+        uint16_t* aw = w.aw + pr * AW_ELEMS + (size_t)row * D + 32 * grp;
+        float* uu = w.uu + pr * UU_FLOATS + (size_t)row * D + 32 * grp;
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= up;
+            st_stream_f8(uu + c, v);
+            st_stream_f8(uu + c + 8, v + 8);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= up;
+            st_stream_h16(aw + c, v);
+        }
+    };
+    long prec = -1;   // the previous record, whose output rows are still to be written
+
     for (; rec < w.nrec; rec += stride) {
+        if (prec >= 0 && row >= C) write_a_rows(prec);
         const bool has_next = rec + stride < w.nrec;
         cur = Loc{s_loc[0], s_loc[1], s_loc[2], s_loc[6]};
         const Loc nxt = has_next ? Loc{s_loc[3], s_loc[4], s_loc[5], s_loc[7]} : cur;
@@ -390,8 +460,11 @@ prep_kernel(kda_prefill_args a, Work w,
         // ---- 1a. q/k L2 norms: threads 2v and 2v+1 cover vector v (q of token v for
         //          v < 64, else k of token v - 64), 64 dims each, reading 16-byte chunks in
         //          a rotated order so that each quarter-warp hits 8 distinct bank groups
-        if (tid < 2 * D) {
-            const int v = tid >> 1, half = tid & 1;
+        //          (the warps of TMEM lanes 0..63; the others write the previous
+        //          record's output rows meanwhile)
+        if (quad < 2) {
+            const int i1a = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;
+            const int v = i1a >> 1, half = i1a & 1;
             const int t = v & (C - 1);
             const uint16_t* rowp = (v < C ? sRawQ : sRawK) + t * D + half * (D / 2);
             float ssum = 0.f;
@@ -780,19 +853,21 @@ prep_kernel(kda_prefill_args a, Work w,
             load_qkz(nxt);
         }
 
-        // ---- 6. the record: [U ; U_o] and [-W ; Gamma Q - P Gamma K] (row = lane, 32 columns)
+        // ---- 6. the record: U and -W (row = lane, 32 columns); the output rows U_o and
+        //      Gamma Q - P Gamma K of the A tile follow at the start of the next record
+        //      (write_a_rows), once every thread's part of the rows' largest entries is in
         {
             float v[16];
             float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 32 * grp;
             uint16_t* aw = w.aw + rec * AW_ELEMS + (size_t)row * D + 32 * grp;
-#pragma unroll
-            for (int c = 0; c < 32; c += 16) {
-                tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
-                tc::tmem_ld_wait();
-                st_stream_f8(uu + c, v);
-                st_stream_f8(uu + c + 8, v + 8);
-            }
             if (row < C) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 16) {
+                    tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
+                    tc::tmem_ld_wait();
+                    st_stream_f8(uu + c, v);
+                    st_stream_f8(uu + c + 8, v + 8);
+                }
 #pragma unroll
                 for (int c = 0; c < 32; c += 16) {
                     tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
@@ -802,25 +877,22 @@ prep_kernel(kda_prefill_args a, Work w,
                     st_stream_h16(aw + c, v);
                 }
             } else {
-                const int t = row - C;
-                const float* es = s_expS + (t >> 4) * D;
+                // the row back into TMEM in place of P Gamma K, for write_a_rows
+                float ma = 0.f, mu = 0.f;
 #pragma unroll
                 for (int c = 0; c < 32; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
-                    tc::tmem_ld_wait();
-                    float o4[16];
+                    a_row(c, v);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const int d = 32 * grp + c + j;
-                        const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
-                        const float4 e4 = *reinterpret_cast<const float4*>(es + d);
-                        o4[j] = q4.x * e4.x - v[j];
-                        o4[j + 1] = q4.y * e4.y - v[j + 1];
-                        o4[j + 2] = q4.z * e4.z - v[j + 2];
-                        o4[j + 3] = q4.w * e4.w - v[j + 3];
-                    }
-                    st_stream_h16(aw + c, o4);
+                    for (int j = 0; j < 16; ++j) ma = fmaxf(ma, fabsf(v[j]));
+                    tc::tmem_st16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+                    tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) mu = fmaxf(mu, fabsf(v[j]));
                 }
+                s_rmax[grp * C + row - C] = ma;
+                s_rmax[4 * C + grp * C + row - C] = mu;
+                tc::tmem_st_wait();
             }
             tc::fence_before_sync();
         }
@@ -843,8 +915,10 @@ prep_kernel(kda_prefill_args a, Work w,
             *reinterpret_cast<long*>(s_loc + 8) = g;
             s_loc[10] = hh;
         }
+        prec = rec;
         __syncthreads();
     }
+    if (prec >= 0 && row >= C) write_a_rows(prec);
     // give-up path: wait for the copies and the MMA thread 0 issued before any
     // of this CTA's shared memory or TMEM is released
     if (__syncthreads_or(timed_out) && tid == 0) {
@@ -884,10 +958,10 @@ struct ScanCfg {
     static constexpr int OFF_GF0 = OFF_K1 + KT_BYTES;        // one tile per chunk parity
     static constexpr int OFF_GF1 = OFF_GF0 + GF_TILE;
     // [U ; U_o] rows of a chunk (the CTA's NE columns, SW128 fp32 [128 rows][NE]) and
-    // gamma_C (128 floats) by TMA into a ring of NU buffers, loaded two chunks ahead
+    // [gamma_C ; rho] (192 floats) by TMA into a ring of NU buffers, loaded two chunks ahead
     static constexpr int NU = 3;
     static constexpr int U_TILE = 128 * NE * 4;
-    static constexpr int U_BUF = U_TILE + 128 * 4;
+    static constexpr int U_BUF = U_TILE + (int)GM_FLOATS * 4;
     static constexpr int OFF_U = (OFF_GF1 + GF_TILE + 1023) / 1024 * 1024;
     static constexpr int OFF_SMALL = OFF_U + NU * ((U_BUF + 1023) / 1024 * 1024);
     // small region (floats): peers' row sums of squares [2 parity][R source][C], this
@@ -986,7 +1060,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
     // with v = 0 takes 2^c_e from S0 alone.  In a transition scan (TRANS: v = 0, the
     // state only decays or mixes) x_j, one exponent for the CTA's columns, follows
     // the largest |S| chunk by chunk, so that the state's fp16 copy stays near 1
-    // however fast it decays; otherwise x_j = 0.  (Terms below 2^-24 of the record
+    // however fast it decays; otherwise x_j = 0.  An output row of the A tile whose
+    // entries are all small comes raised by 1 / rho (prep's row scaling), so the row's
+    // sum is multiplied by rho on the way out.  (Terms below 2^-24 of the record
     // operands' own scale -- a chunk's contraction terms under very fast decay --
     // are lost to fp16 whatever x: a transition matrix is exact to about 2^-24 of
     // |S0|, not relative to itself once it has decayed below that.)
@@ -1133,9 +1209,9 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             auto load_u = [&](int j) {   // chunk j's U rows (this CTA's columns) and gamma_C
                 const int k = j % Cfg::NU;
                 ++n_u[k];
-                tc::mbar_arrive_expect_tx(bar_u + k, (w.zero_v ? 0 : Cfg::U_TILE) + 128 * 4);
+                tc::mbar_arrive_expect_tx(bar_u + k, (w.zero_v ? 0 : Cfg::U_TILE) + (uint32_t)GM_FLOATS * 4);
                 if (!w.zero_v) tc::tma_load_2d(u_buf(k), &tm_uu, NE * r, (int)(rec_of(j) * 128), bar_u + k);
-                tc::bulk_load(u_buf(k) + Cfg::U_TILE, w.gm + rec_of(j) * GM_FLOATS, 128 * 4, bar_u + k);
+                tc::bulk_load(u_buf(k) + Cfg::U_TILE, w.gm + rec_of(j) * GM_FLOATS, (uint32_t)GM_FLOATS * 4, bar_u + k);
             };
             for (int j = 0; j < Cfg::NU && j < nch; ++j) load_u(j);
             for (int j = 0; j < 2 && j < nch; ++j) { load_aw(j); load_k(j); }
@@ -1201,13 +1277,20 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         nbar_sync(NB_S, NS);       // the epilogue's last arrival
     } else {
         // ------------------------------------------------------------------ epilogue
+        // this thread's columns' scale factors 2^-c and 2^c, kept in registers
+        float vsc_r[HW], vinv_r[HW];
+#pragma unroll
+        for (int c = 0; c < HW; ++c) { vsc_r[c] = s_vsc[c_lo + c]; vinv_r[c] = s_vinv[c_lo + c]; }
         // chunk j's record rows from U-ring buffer j % NU into TMEM buffer j & 1
         // ([U ; U_o] row `row`, this thread's HW columns, scaled by 2^-c); returns
-        // gamma_C[row] of the chunk
-        auto store_rec = [&](int j) -> float {
+        // gamma_C[row] of the chunk and, for an output row, rho (the power of two by
+        // which the row's sum comes out too large)
+        auto store_rec = [&](int j) -> float2 {
             const int k = j % Cfg::NU;
             wait(bar_u + k, (j / Cfg::NU) & 1);
             const uint8_t* ub = u_buf(k);
+            const float* gr = reinterpret_cast<const float*>(ub + Cfg::U_TILE);
+            const float rho = vrow ? 1.f : gr[D + row - C];
             if (!w.zero_v) {
 #pragma unroll
                 for (int i = 0; i < HW; i += 16) {
@@ -1215,21 +1298,21 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
 #pragma unroll
                     for (int q = 0; q < 16; q += 4) {
                         const float4 u4 = *reinterpret_cast<const float4*>(ub + sw128_f32(row, c_lo + i + q));
-                        v[q] = u4.x * s_vsc[c_lo + i + q];
-                        v[q + 1] = u4.y * s_vsc[c_lo + i + q + 1];
-                        v[q + 2] = u4.z * s_vsc[c_lo + i + q + 2];
-                        v[q + 3] = u4.w * s_vsc[c_lo + i + q + 3];
+                        v[q] = u4.x * vsc_r[i + q];
+                        v[q + 1] = u4.y * vsc_r[i + q + 1];
+                        v[q + 2] = u4.z * vsc_r[i + q + 2];
+                        v[q + 3] = u4.w * vsc_r[i + q + 3];
                     }
                     tc::tmem_st16(T0 + Cfg::TM_D + NE * (j & 1) + lane_base + c_lo + i, v);
                 }
             }
-            const float g = reinterpret_cast<const float*>(ub + Cfg::U_TILE)[row];
+            const float2 g = make_float2(gr[row], rho);
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_ufree + k);
             return g;
         };
         // o and y of chunk jo from its TMEM buffer (output-row threads)
-        auto emit_outputs = [&](int jo, int xo) {   // xo: the chunk's exponent
+        auto emit_outputs = [&](int jo, int xo, float rho_o) {   // the chunk's exponent, the row's rho
             const int bo = jo & 1;
             const int t = row - C;
             const int c0o = t_begin + C * jo;
@@ -1238,8 +1321,12 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
 #pragma unroll
             for (int c = 0; c < HW; c += 16) tc::tmem_ld16(T0 + Cfg::TM_D + NE * bo + lane_base + c_lo + c, o + c);
             tc::tmem_ld_wait();
+            if (rho_o != 1.f) {
 #pragma unroll
-            for (int c = 0; c < HW; ++c) o[c] *= a.scale * s_vinv[c_lo + c] * exp2i(-xo);
+                for (int c = 0; c < HW; ++c) o[c] *= rho_o;
+            }
+#pragma unroll
+            for (int c = 0; c < HW; ++c) o[c] *= a.scale * vinv_r[c] * exp2i(-xo);
             if (t < nco && a.o) {
                 if (din == D) {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(a.o) + ((size_t)(c0o + t) * H + h) * D + NE * r + c_lo;
@@ -1277,7 +1364,8 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
         };
 
         // ---- initial state -> TMEM master copy and the fp16 operand copy
-        float gm_next = 0.f;   // gamma_C of the next chunk, one chunk ahead
+        float2 gm_next = make_float2(0.f, 1.f);   // gamma_C and rho of the next chunk, one chunk ahead
+        float rho_prev = 1.f;                     // rho of the previous chunk
         int x_prev = 0, x_cur = 0, x_next = 0;   // the exponent x of the previous, this, the next chunk
         {
             const int d = row;
@@ -1305,13 +1393,13 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             const int b = j & 1;
             const int c0 = t_begin + C * j;
             const int nc = min(C, t_end - c0);
-            const float gm = gm_next;
+            const float gm = gm_next.x, rho = gm_next.y;
 
             // ---- while MMA 2 runs: outputs of the previous chunk (their buffer is
             //      refilled next), the next record into the other TMEM buffer, the one
             //      after it into registers
             if (!vrow) {
-                if (j > 0 && (a.o || gate)) emit_outputs(j - 1, x_prev);
+                if (j > 0 && (a.o || gate)) emit_outputs(j - 1, x_prev, rho_prev);
                 // arm this chunk's exchange barrier (its phase for chunk j - 2 completed:
                 // this thread waited for it in emit_outputs; a peer that stopped leaves
                 // it open, and then it is not armed again)
@@ -1348,9 +1436,13 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
                 for (int c = c_lo; c < c_lo + HW; c += 16) {
                     tc::tmem_ld16(T0 + Cfg::TM_D + NE * b + lane_base + c, v);
                     tc::tmem_ld_wait();
+                    if (rho != 1.f) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) v[jj] *= rho;
+                    }
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const float x = v[jj] * (s_vinv[c + jj] * exp2i(-x_cur));
+                        const float x = v[jj] * (vinv_r[c - c_lo + jj] * exp2i(-x_cur));
                         ss = fmaf(x, x, ss);
                     }
                 }
@@ -1472,9 +1564,10 @@ scan_kernel(kda_prefill_args a, Work w, const __grid_constant__ CUtensorMap tm_a
             nbar_sync(NB_S, NS);
             x_prev = x_cur;
             x_cur = x_next;
+            rho_prev = rho;
         }
         // outputs of the last chunk
-        if (nch > 0 && !vrow && (a.o || gate)) emit_outputs(nch - 1, x_prev);
+        if (nch > 0 && !vrow && (a.o || gate)) emit_outputs(nch - 1, x_prev, rho_prev);
 
         // ---- final state
         if (a.S_T) {
