@@ -193,7 +193,10 @@ TC_DEV float warp_reduce_scatter32(float (&v)[32], int lane) {
 // ---------------------------------------------------------------------------
 namespace prep {
 // Region RB, in turn: the raw q, k, z tiles; the Gram's B operand (the key versions);
-// the Gram tiles and the solve's scratch; B_pre = [V | Gamma K]^T.
+// the Gram tiles and the solve's scratch; then, from the end of the solve, the next
+// record's raw q, k, z.  B_pre = [V | Gamma K]^T, MMA 1's B operand, comes in two
+// halves: V^T in region QK once the Gram has read [Q~ ; K~], (Gamma K)^T in a region
+// of its own, written while the Gram runs.
 constexpr int KV_ROWS = 160;                        // key versions: 16 (a + 1) rows for a = 0..3
 constexpr int RB_BYTES = KV_ROWS * D * 4;           // 80 KB
 constexpr int OFF_RB = 0;
@@ -203,10 +206,11 @@ constexpr int OFF_RAWZ = OFF_RB + 2 * C * D * 2;    // [C][D] f32
 constexpr int OFF_KV = OFF_RB;                      // SW128 [160 rows][D]
 constexpr int OFF_AQK = OFF_RB;
 constexpr int OFF_AKK = OFF_RB + C * AS * 4;
-constexpr int OFF_BPRE = OFF_RB;                    // SW128 [256 rows][C]
 constexpr int OFF_QK = OFF_RB + RB_BYTES;           // the Gram's A operand [Q~ ; K~], SW128 [128 rows][D]
+constexpr int OFF_BPRE = OFF_QK;                    // V^T, SW128 [128 rows][C]
 constexpr int OFF_RAWV = OFF_QK + 2 * C * D * 4;    // two [C][64] bf16 tiles, 128-B swizzle
-constexpr int OFF_SMALL = OFF_RAWV + 2 * C * 64 * 2;
+constexpr int OFF_GK = OFF_RAWV + 2 * C * 64 * 2;   // (Gamma K)^T, SW128 [128 rows][C]
+constexpr int OFF_SMALL = OFF_GK + D * C * 4;
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
               SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
               SM_DIAG = SM_CTAB + NPAIR * D,            // [4 sub-chunks][9 batches][4 warps][32]
@@ -215,9 +219,9 @@ constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_T
               SM_FLOATS = SM_LOC + 16;
 constexpr int EA_HEADS = 128;
 constexpr int SMEM_BYTES = OFF_SMALL + SM_FLOATS * 4 + 64 + 1024;
-static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0 && OFF_QK % 1024 == 0 && OFF_KV % 1024 == 0,
-              "swizzled tiles need 1024-B alignment");
-static_assert(2 * D * C * 4 <= RB_BYTES && 2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
+static_assert(OFF_RAWV % 1024 == 0 && OFF_BPRE % 1024 == 0 && OFF_QK % 1024 == 0 && OFF_KV % 1024 == 0 &&
+              OFF_GK % 1024 == 0, "swizzled tiles need 1024-B alignment");
+static_assert(2 * C * D * 2 + C * D * 4 <= RB_BYTES, "region RB");
 static_assert(3 * C * AS * 4 + (NT / 32) * 16 * 16 * 4 <= RB_BYTES, "region RB holds the solve tiles");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t BYTES_QKZ = 2 * C * D * 2 + C * D * 4;
@@ -226,7 +230,7 @@ constexpr uint32_t BYTES_V = C * D * 2;
 // slots (q, k, z: 16 KB at most each, v: 16 KB at most); channels DIN..127 read as 0
 constexpr int DIN_MAX = 64;
 constexpr int NTP = 512;         // threads per CTA (16 warps; warps w, w+4, w+8, w+12 share TMEM lanes)
-constexpr uint32_t TM_D = 0;     // 256 cols: [U | W ; U_o | P Gamma K]
+constexpr uint32_t TM_D = 0;     // 256 cols: [U | W ; U_o | P Gamma K - Gamma Q]
 constexpr uint32_t TM_A2 = 256;  // 64 cols: [T beta ; P beta]
 constexpr uint32_t TM_G = 320;   // 160 cols: [Q~ ; K~] . (key versions)^T
 constexpr uint32_t TM_COLS = 512;
@@ -248,6 +252,7 @@ prep_kernel(kda_prefill_args a, Work w,
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sBpre = sm + OFF_BPRE;
+    uint8_t* sGK = sm + OFF_GK;
     const uint16_t* sRawQ = reinterpret_cast<const uint16_t*>(sm + OFF_RAWQ);
     const uint16_t* sRawK = reinterpret_cast<const uint16_t*>(sm + OFF_RAWK);
     const float* sRawZ = reinterpret_cast<const float*>(sm + OFF_RAWZ);
@@ -374,25 +379,6 @@ prep_kernel(kda_prefill_args a, Work w,
     float beta_next = 0.f;
     if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
 
-    // The output rows (row >= C) of a record's A tile, Gamma Q - P Gamma K: 16 of the
-    // row's columns of this thread into v, from TMEM (P Gamma K) and shared memory (q~
-    // and the sub-chunk decays).
-    auto a_row = [&](int c, float* v) {
-        const int t = row - C;
-        const float* es = s_expS + ((t & (C - 1)) >> 4) * D;
-        tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const int d = 32 * grp + c + j;
-            const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
-            const float4 e4 = *reinterpret_cast<const float4*>(es + d);
-            v[j] = q4.x * e4.x - v[j];
-            v[j + 1] = q4.y * e4.y - v[j + 1];
-            v[j + 2] = q4.z * e4.z - v[j + 2];
-            v[j + 3] = q4.w * e4.w - v[j + 3];
-        }
-    };
     // the four column groups' largest |A| and |U_o| of each output row, from phase 6 of
     // a record to phase 1b of the next (the diagonal-block buffer is free in between)
     float* s_rmax = s_diag;
@@ -403,9 +389,9 @@ prep_kernel(kda_prefill_args a, Work w,
     // is not small.  A row whose largest entry is below 2^-7 is raised to [1/2, 1) (by
     // at most 2^96, and U_o's row stays below 2^120); the others keep s_t = 0, rho_t = 1
     // (their entries below the fp16 normals are under 2^-7 of the row's largest).
-    // Phase 6 leaves the A rows in TMEM (in place of P Gamma K) beside U_o; this runs at
-    // the start of the next record, while the others compute the L2 norms, so that no
-    // barrier of its own is needed.
+    // The rows wait in TMEM (as P Gamma K - Gamma Q, minus the A tile's rows) beside U_o;
+    // this runs at the start of the next record, while the others compute the L2 norms,
+    // so that no barrier of its own is needed.
     auto write_a_rows = [&](long pr) {
         tc::fence_after_sync();
         const int t = row - C;
@@ -437,7 +423,7 @@ prep_kernel(kda_prefill_args a, Work w,
             tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= up;
+            for (int j = 0; j < 16; ++j) v[j] *= -up;
             st_stream_h16(aw + c, v);
         }
     };
@@ -607,6 +593,18 @@ prep_kernel(kda_prefill_args a, Work w,
 #pragma unroll
             for (int u = 0; u < 16; ++u) k16[u] = kf2[u] * ec;
             st_stream_h16(w.kt + rec * KT_ELEMS + (size_t)d * C + 16 * b, k16);
+            // (Gamma K)^T, MMA 1's second B operand: row d, the 16 tokens of sub-chunk b
+            const float es = s_expS[b * D + d];
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+                const int t = 16 * b + i;
+                float4 w4;
+                w4.x = tc::to_tf32(qk_at(C + t, d) * es);
+                w4.y = tc::to_tf32(qk_at(C + t + 1, d) * es);
+                w4.z = tc::to_tf32(qk_at(C + t + 2, d) * es);
+                w4.w = tc::to_tf32(qk_at(C + t + 3, d) * es);
+                *reinterpret_cast<float4*>(sGK + tc::sw128_offset(d, t, D)) = w4;
+            }
             tc::fence_proxy_async();
         }
         __syncthreads();
@@ -619,6 +617,34 @@ prep_kernel(kda_prefill_args a, Work w,
                 tc::mma_tf32_ss(T0 + TM_G, tc::sw128_desc_k(ab, 2 * C, ks), tc::sw128_desc_k(bb, KV_ROWS, ks),
                                 tc::idesc_tf32(2 * C, KV_ROWS), ks > 0);
             tc::mma_commit(mbar);
+        }
+        // while the Gram runs: D[:, 128:256] <- [0 ; -Gamma Q], onto which MMA 1 adds
+        // [T beta ; P beta] . Gamma K (the output rows then hold minus the A tile's rows)
+        {
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                if (row >= C) {
+                    const int t = row - C;
+                    const float* es = s_expS + (t >> 4) * D;
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const int d = 32 * grp + c + j;
+                        const float4 q4 = *reinterpret_cast<const float4*>(&qk_at(t, d));
+                        const float4 e4 = *reinterpret_cast<const float4*>(es + d);
+                        v[j] = -(q4.x * e4.x);
+                        v[j + 1] = -(q4.y * e4.y);
+                        v[j + 2] = -(q4.z * e4.z);
+                        v[j + 3] = -(q4.w * e4.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                }
+                tc::tmem_st16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+            }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
         }
         wait(mbar, ph_mma);
         ph_mma ^= 1u;
@@ -784,42 +810,35 @@ prep_kernel(kda_prefill_args a, Work w,
             }
         }
         __syncthreads();   // the Gram tiles are dead from here on
+        // region RB is free: fetch the next record's q, k, z into it
+        if (tid == 0 && has_next && !timed_out) {
+            ++n_in;
+            tc::fence_proxy_async();
+            load_qkz(nxt);
+        }
         wait(bar_v, ph_v);
         ph_v ^= 1u;
 
-        // ---- 4. B_pre = [V | Gamma K]^T (256 rows) and the record's gamma_C
+        // ---- 4. V^T (B_pre's first half, in region QK: the Gram has read it) and the
+        //         record's gamma_C (thread: value column e, a quarter of the tokens)
         {
-            const int rr = tid & (2 * D - 1), th = tid >> 8;   // B_pre row, half of the tokens
-            if (rr < D) {                        // rows 0..127: value columns
-                const int e = rr;
-                float vm = 0.f;   // max |v| of this column over the half's tokens
-#pragma unroll 4
-                for (int t = 32 * th; t < 32 * th + 32; t += 4) {
-                    float4 w4;
-                    float* wp = &w4.x;
+            const int e = tid & (D - 1), th = tid >> 7;
+            float vm = 0.f;   // max |v| of this column over the quarter's tokens
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        wp[u] = (t + u < nc) ? raw_v(t + u, e) : 0.f;
-                        vm = fmaxf(vm, fabsf(wp[u]));
-                    }
-                    *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, 2 * D)) = w4;
-                }
-                // the sequence's column maximum, for the scan's operand scaling
-                // (non-negative floats order like their bit patterns)
-                if (vm > 0.f) atomicMax(w.vmax + ((size_t)cur.n * H + h) * D + e, __float_as_int(vm));
-                if (th == 0) w.gm[rec * GM_FLOATS + e] = s_gam[e];
-            } else {                             // rows 128..255: (Gamma K)^T
-                const int d = rr - D;
-#pragma unroll 4
-                for (int t = 32 * th; t < 32 * th + 32; t += 4) {
-                    float4 w4;
-                    float* wp = &w4.x;
-                    const float es = s_expS[(t >> 4) * D + d];
+            for (int t = 16 * th; t < 16 * th + 16; t += 4) {
+                float4 w4;
+                float* wp = &w4.x;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) wp[u] = tc::to_tf32(qk_at(C + t + u, d) * es);
-                    *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(D + d, t, 2 * D)) = w4;
+                for (int u = 0; u < 4; ++u) {
+                    wp[u] = (t + u < nc) ? raw_v(t + u, e) : 0.f;
+                    vm = fmaxf(vm, fabsf(wp[u]));
                 }
+                *reinterpret_cast<float4*>(sBpre + tc::sw128_offset(e, t, D)) = w4;
             }
+            // the sequence's column maximum, for the scan's operand scaling
+            // (non-negative floats order like their bit patterns)
+            if (vm > 0.f) atomicMax(w.vmax + ((size_t)cur.n * H + h) * D + e, __float_as_int(vm));
+            if (th == 0) w.gm[rec * GM_FLOATS + e] = s_gam[e];
             tc::tmem_st_wait();
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -832,26 +851,24 @@ prep_kernel(kda_prefill_args a, Work w,
             load_v(nxt);
         }
 
-        // ---- 5. MMA 1: D[:, 0:256] = [T beta ; P beta] . [V | Gamma K]
+        // ---- 5. MMA 1: D[:, 0:128] = [T beta ; P beta] . V, D[:, 128:256] += [T beta ; P beta] . Gamma K
         if (tid == 0 && !timed_out) {
             ++n_mma;
             tc::fence_after_sync();
-            const uint32_t bb = tc::smem_u32(sBpre);
+            const uint32_t bv = tc::smem_u32(sBpre), bk = tc::smem_u32(sGK);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(T0 + TM_D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bb, 2 * D, ks),
-                                tc::idesc_tf32(128, 2 * D), ks > 0);
+                tc::mma_tf32_ts(T0 + TM_D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bv, D, ks),
+                                tc::idesc_tf32(128, D), ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(T0 + TM_D + D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bk, D, ks),
+                                tc::idesc_tf32(128, D), 1u);
             tc::mma_commit(mbar);
         }
         wait(mbar, ph_mma);
         ph_mma ^= 1u;
         tc::fence_after_sync();
-        // region RB is free again: fetch the next record's q, k, z into it
-        if (tid == 0 && has_next && !timed_out) {
-            ++n_in;
-            tc::fence_proxy_async();
-            load_qkz(nxt);
-        }
 
         // ---- 6. the record: U and -W (row = lane, 32 columns); the output rows U_o and
         //      Gamma Q - P Gamma K of the A tile follow at the start of the next record
@@ -877,14 +894,14 @@ prep_kernel(kda_prefill_args a, Work w,
                     st_stream_h16(aw + c, v);
                 }
             } else {
-                // the row back into TMEM in place of P Gamma K, for write_a_rows
+                // the rows' largest |A| (TMEM holds -A) and |U_o|, for write_a_rows
                 float ma = 0.f, mu = 0.f;
 #pragma unroll
                 for (int c = 0; c < 32; c += 16) {
-                    a_row(c, v);
+                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+                    tc::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) ma = fmaxf(ma, fabsf(v[j]));
-                    tc::tmem_st16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
                     tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
                     tc::tmem_ld_wait();
 #pragma unroll
@@ -892,7 +909,6 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
                 s_rmax[grp * C + row - C] = ma;
                 s_rmax[4 * C + grp * C + row - C] = mu;
-                tc::tmem_st_wait();
             }
             tc::fence_before_sync();
         }
