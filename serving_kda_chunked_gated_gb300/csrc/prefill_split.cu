@@ -247,7 +247,8 @@ template <int GATE, int IN32>
 __global__ void __launch_bounds__(prep::NTP, 1)
 prep_kernel(kda_prefill_args a, Work w,
             const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v) {
+            const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_v,
+            const __grid_constant__ CUtensorMap tm_uu, const __grid_constant__ CUtensorMap tm_aw) {
     using namespace prep;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -379,58 +380,18 @@ prep_kernel(kda_prefill_args a, Work w,
     float beta_next = 0.f;
     if (rec < w.nrec && tid < C && tid < cur.nc) beta_next = a.beta[(size_t)(cur.t0 + tid) * H + cur.h];
 
-    // the four column groups' largest |A| and |U_o| of each output row, from phase 6 of
-    // a record to phase 1b of the next (the diagonal-block buffer is free in between)
+    // the four column groups' largest |A| and |U_o| of each output row (phase 6; the
+    // diagonal-block buffer is free then)
     float* s_rmax = s_diag;
-    // Output row t of record pr's A tile and of its U_o are stored times 2^s_t, and
-    // rho_t = 2^-s_t goes with gamma_C; the scan multiplies the row's sum back by rho_t.
-    // A row whose every decay factor is small would otherwise sit among the fp16
-    // subnormals and keep only a few bits, and times a large state its product with S
-    // is not small.  A row whose largest entry is below 2^-7 is raised to [1/2, 1) (by
-    // at most 2^96, and U_o's row stays below 2^120); the others keep s_t = 0, rho_t = 1
-    // (their entries below the fp16 normals are under 2^-7 of the row's largest).
-    // The rows wait in TMEM (as P Gamma K - Gamma Q, minus the A tile's rows) beside U_o;
-    // this runs at the start of the next record, while the others compute the L2 norms,
-    // so that no barrier of its own is needed.
-    auto write_a_rows = [&](long pr) {
-        tc::fence_after_sync();
-        const int t = row - C;
-        const float ma = fmaxf(fmaxf(s_rmax[t], s_rmax[C + t]), fmaxf(s_rmax[2 * C + t], s_rmax[3 * C + t]));
-        const float* sm2 = s_rmax + 4 * C;
-        const float mu = fmaxf(fmaxf(sm2[t], sm2[C + t]), fmaxf(sm2[2 * C + t], sm2[3 * C + t]));
-        // m = f 2^e with f in [1/2, 1): e from the exponent bits (a subnormal ma reads
-        // as e = -126, beyond the cap); U_o's row stays below 2^120
-        const int eu = (mu > 0.f && mu <= 3.0e38f) ? (int)((__float_as_uint(mu) >> 23) & 0xffu) - 126 : 0;
-        const int st = (ma > 0.f && ma < 0.0078125f)
-                           ? max(0, min(min(96, 126 - (int)((__float_as_uint(ma) >> 23) & 0xffu)), 120 - eu))
-                           : 0;
-        const float up = __int_as_float((127 + st) << 23);
-        if (grp == 0) w.gm[pr * GM_FLOATS + D + t] = __int_as_float((127 - st) << 23);
-        uint16_t* aw = w.aw + pr * AW_ELEMS + (size_t)row * D + 32 * grp;
-        float* uu = w.uu + pr * UU_FLOATS + (size_t)row * D + 32 * grp;
-        float v[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-            tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= up;
-            st_stream_f8(uu + c, v);
-            st_stream_f8(uu + c + 8, v + 8);
-        }
-#pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-            tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] *= -up;
-            st_stream_h16(aw + c, v);
-        }
-    };
-    long prec = -1;   // the previous record, whose output rows are still to be written
+    // the record's TMA stores are issued and awaited by a thread that has no part in the
+    // L2 norms (step 1a), so that the wait for the previous record's stores overlaps them
+    constexpr int TID_ST = NTP - 32;
+    bool stores_out = false;   // thread TID_ST: the previous record's A-tile store may still read its tile
 
     for (; rec < w.nrec; rec += stride) {
-        if (prec >= 0 && row >= C) write_a_rows(prec);
+        // the previous record's [U ; U_o] tile (region QK) is rewritten in 1b, its A tile
+        // (the (Gamma K)^T region) in step 2: their stores, in that order, in two groups
+        if (tid == TID_ST && stores_out) tc::bulk_wait_read_but1();
         const bool has_next = rec + stride < w.nrec;
         cur = Loc{s_loc[0], s_loc[1], s_loc[2], s_loc[6]};
         const Loc nxt = has_next ? Loc{s_loc[3], s_loc[4], s_loc[5], s_loc[7]} : cur;
@@ -446,11 +407,8 @@ prep_kernel(kda_prefill_args a, Work w,
         // ---- 1a. q/k L2 norms: threads 2v and 2v+1 cover vector v (q of token v for
         //          v < 64, else k of token v - 64), 64 dims each, reading 16-byte chunks in
         //          a rotated order so that each quarter-warp hits 8 distinct bank groups
-        //          (the warps of TMEM lanes 0..63; the others write the previous
-        //          record's output rows meanwhile)
-        if (quad < 2) {
-            const int i1a = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;
-            const int v = i1a >> 1, half = i1a & 1;
+        if (tid < 2 * D) {
+            const int v = tid >> 1, half = tid & 1;
             const int t = v & (C - 1);
             const uint16_t* rowp = (v < C ? sRawQ : sRawK) + t * D + half * (D / 2);
             float ssum = 0.f;
@@ -567,6 +525,7 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
             }
         }
+        if (tid == TID_ST && stores_out) { tc::bulk_wait_read(); stores_out = false; }
         __syncthreads();
 
         // ---- 2. Gram sub-blocks on the tensor cores.  Block (a, b), b <= a, of A_qk and A_kk is
@@ -870,31 +829,22 @@ prep_kernel(kda_prefill_args a, Work w,
         ph_mma ^= 1u;
         tc::fence_after_sync();
 
-        // ---- 6. the record: U and -W (row = lane, 32 columns); the output rows U_o and
-        //      Gamma Q - P Gamma K of the A tile follow at the start of the next record
-        //      (write_a_rows), once every thread's part of the rows' largest entries is in
+        // ---- 6. the record: [U ; U_o] (fp32) and [-W ; Gamma Q - P Gamma K] (fp16; TMEM
+        //      holds its negative) into shared memory as SW128 tiles -- [U ; U_o] in region
+        //      QK, the A tile in the (Gamma K)^T region, both free once MMA 1 has read them
+        //      -- and out by TMA (row = lane, 32 columns).  Output row t of both is stored
+        //      times 2^s_t, s_t >= 0, and rho_t = 2^-s_t goes with gamma_C: a row whose every
+        //      decay factor is small would otherwise sit among the fp16 subnormals and keep
+        //      only a few bits, and times a large state its product with S is not small.  A
+        //      row whose largest entry is below 2^-7 is raised to [1/2, 1) (by at most 2^96,
+        //      and U_o's row stays below 2^120); the others keep s_t = 0, rho_t = 1 (their
+        //      entries below the fp16 normals are under 2^-7 of the row's largest).  The scan
+        //      multiplies the row's sum back by rho_t.
         {
             float v[16];
-            float* uu = w.uu + rec * UU_FLOATS + (size_t)row * D + 32 * grp;
-            uint16_t* aw = w.aw + rec * AW_ELEMS + (size_t)row * D + 32 * grp;
-            if (row < C) {
-#pragma unroll
-                for (int c = 0; c < 32; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
-                    tc::tmem_ld_wait();
-                    st_stream_f8(uu + c, v);
-                    st_stream_f8(uu + c + 8, v + 8);
-                }
-#pragma unroll
-                for (int c = 0; c < 32; c += 16) {
-                    tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = -v[j];
-                    st_stream_h16(aw + c, v);
-                }
-            } else {
-                // the rows' largest |A| (TMEM holds -A) and |U_o|, for write_a_rows
+            uint8_t* sU = sm + OFF_QK;
+            uint8_t* sA = sGK;
+            if (row >= C) {   // the row's largest |A| and |U_o|, this thread's 32 columns
                 float ma = 0.f, mu = 0.f;
 #pragma unroll
                 for (int c = 0; c < 32; c += 16) {
@@ -910,7 +860,56 @@ prep_kernel(kda_prefill_args a, Work w,
                 s_rmax[grp * C + row - C] = ma;
                 s_rmax[4 * C + grp * C + row - C] = mu;
             }
+            __syncthreads();
+            float up = 1.f;   // 2^s_t
+            if (row >= C) {
+                const int t = row - C;
+                const float ma = fmaxf(fmaxf(s_rmax[t], s_rmax[C + t]), fmaxf(s_rmax[2 * C + t], s_rmax[3 * C + t]));
+                const float* sm2 = s_rmax + 4 * C;
+                const float mu = fmaxf(fmaxf(sm2[t], sm2[C + t]), fmaxf(sm2[2 * C + t], sm2[3 * C + t]));
+                // m = f 2^e with f in [1/2, 1): e from the exponent bits (a subnormal ma
+                // reads as e = -126, beyond the cap)
+                const int eu = (mu > 0.f && mu <= 3.0e38f) ? (int)((__float_as_uint(mu) >> 23) & 0xffu) - 126 : 0;
+                const int st = (ma > 0.f && ma < 0.0078125f)
+                                   ? max(0, min(min(96, 126 - (int)((__float_as_uint(ma) >> 23) & 0xffu)), 120 - eu))
+                                   : 0;
+                up = __int_as_float((127 + st) << 23);
+                if (grp == 0) w.gm[rec * GM_FLOATS + D + t] = __int_as_float((127 - st) << 23);
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                tc::tmem_ld16(T0 + TM_D + lane_base + 32 * grp + c, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4*>(sU + tc::sw128_offset(row, 32 * grp + c + j, 128)) =
+                        make_float4(v[j] * up, v[j + 1] * up, v[j + 2] * up, v[j + 3] * up);
+            }
+            const float nup = -up;
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                tc::tmem_ld16(T0 + TM_D + lane_base + D + 32 * grp + c, v);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; j += 8)
+                    *reinterpret_cast<uint4*>(sA + tc::sw128_offset_h(row, 32 * grp + c + j, 128)) =
+                        make_uint4(tc::pack_f16x2(v[j] * nup, v[j + 1] * nup), tc::pack_f16x2(v[j + 2] * nup, v[j + 3] * nup),
+                                   tc::pack_f16x2(v[j + 4] * nup, v[j + 5] * nup), tc::pack_f16x2(v[j + 6] * nup, v[j + 7] * nup));
+            }
+            tc::fence_proxy_async();
             tc::fence_before_sync();
+        }
+        __syncthreads();
+        if (tid == TID_ST && !timed_out) {
+            uint8_t* sU = sm + OFF_QK;
+            const int y = (int)(rec * 128);
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) tc::tma_store_2d(&tm_uu, 32 * sl, y, sU + sl * (128 * 128));
+            tc::bulk_commit();
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) tc::tma_store_2d(&tm_aw, 64 * sl, y, sGK + sl * (128 * 128));
+            tc::bulk_commit();
+            stores_out = true;
         }
         if (tid == NTP - 1 && has_next) {   // advance the walk: this record <- the next, next <- one stride on
             s_loc[0] = s_loc[3]; s_loc[1] = s_loc[4]; s_loc[2] = s_loc[5]; s_loc[6] = s_loc[7];
@@ -931,10 +930,9 @@ prep_kernel(kda_prefill_args a, Work w,
             *reinterpret_cast<long*>(s_loc + 8) = g;
             s_loc[10] = hh;
         }
-        prec = rec;
         __syncthreads();
     }
-    if (prec >= 0 && row >= C) write_a_rows(prec);
+    if (tid == TID_ST) tc::bulk_wait_all();   // every record store has landed before the CTA exits
     // give-up path: wait for the copies and the MMA thread 0 issued before any
     // of this CTA's shared memory or TMEM is released
     if (__syncthreads_or(timed_out) && tid == 0) {
@@ -1759,7 +1757,7 @@ cudaError_t launch_prefill_split_parts(const kda_prefill_args& a, int parts, int
             const bool sp = a.gate_mode == KDA_GATE_SOFTPLUS, f32 = a.qkv_dtype == KDA_F32;
             auto kern = sp ? (f32 ? spl::prep_kernel<1, 1> : spl::prep_kernel<1, 0>)
                            : (f32 ? spl::prep_kernel<0, 1> : spl::prep_kernel<0, 0>);
-            kern<<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv);
+            kern<<<(unsigned)grid, spl::prep::NTP, spl::prep::SMEM_BYTES, s>>>(a, w, mq, mk, mz, mv, muu, maw);
             ++launched;
         }
     }

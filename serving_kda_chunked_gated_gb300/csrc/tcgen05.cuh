@@ -222,6 +222,19 @@ TC_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(mbar))
         : "memory");
 }
+// TMA: 2-D tiled bulk copy shared -> global, completion tracked by this thread's bulk
+// groups (commit with bulk_commit; bulk_wait_read -- or bulk_wait_read_but1, which
+// leaves the newest group pending -- before a source is rewritten, bulk_wait_all
+// before the CTA exits)
+TC_DEV void tma_store_2d(const void* map, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+TC_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+TC_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+TC_DEV void bulk_wait_read_but1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+TC_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 TC_DEV void tma_prefetch_desc(const void* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
