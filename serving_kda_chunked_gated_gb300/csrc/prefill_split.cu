@@ -707,11 +707,6 @@ prep_kernel(kda_prefill_args a, Work w,
                 store(acc2, blk(sT, a_, b_), AS, -1.f);
                 __syncwarp();
             };
-            auto p_block = [&](float (&acc)[2][4], int a_, int b_) {
-                zero(acc);
-#pragma unroll 1
-                for (int c_ = b_; c_ <= a_; ++c_) mma16(acc, blk(sAqk, a_, c_), blk(sT, c_, b_), AS);
-            };
             if (tid < C) {
                 const int aa = tid >> 4, i = tid & 15;
                 const float* Ad = blk(sAkk, aa, aa);
@@ -729,29 +724,68 @@ prep_kernel(kda_prefill_args a, Work w,
                 for (int j = 0; j < 16; ++j) Td[j] = x[j];
             }
             __syncthreads();
-            float pA[2][4], pB[2][4];
-            if (warp < 3) t_block(warp + 1, warp);
-            else if (warp < 7) p_block(pA, warp - 3, warp - 3);
+            // Off-diagonal blocks by doubling on the 32 x 32 halves: T10 and T32 first,
+            // then Y = A[2:4, 0:2] T[0:2, 0:2] (kept in T's unused upper blocks: Y_ab at
+            // T's block (b, a)), then T[2:4, 0:2] = -T[2:4, 2:4] Y.  P = A_qk T: each of
+            // warps 6..15 owns one P block, accumulated as its T blocks appear and stored
+            // over A_qk's once every A_qk block has been read.  Four levels, the longest
+            // two products deep.
+            float acc[2][4];
+            zero(acc);
+            switch (warp) {   // level 1: T's diagonal blocks are in
+                case 0: t_block(1, 0); break;                                                   // T10
+                case 1: t_block(3, 2); break;                                                   // T32
+                case 2: mma16(acc, blk(sAkk, 2, 1), blk(sT, 1, 1), AS); store(acc, blk(sT, 1, 2), AS, 1.f); break;  // Y21
+                case 3: mma16(acc, blk(sAkk, 3, 1), blk(sT, 1, 1), AS); store(acc, blk(sT, 1, 3), AS, 1.f); break;  // Y31
+                case 4: mma16(acc, blk(sAkk, 2, 0), blk(sT, 0, 0), AS); break;                  // Y20 (part)
+                case 5: mma16(acc, blk(sAkk, 3, 0), blk(sT, 0, 0), AS); break;                  // Y30 (part)
+                case 6: mma16(acc, blk(sAqk, 0, 0), blk(sT, 0, 0), AS); break;                  // P00
+                case 7: mma16(acc, blk(sAqk, 1, 1), blk(sT, 1, 1), AS); break;                  // P11
+                case 8: mma16(acc, blk(sAqk, 2, 2), blk(sT, 2, 2), AS); break;                  // P22
+                case 9: mma16(acc, blk(sAqk, 3, 3), blk(sT, 3, 3), AS); break;                  // P33
+                case 10: mma16(acc, blk(sAqk, 1, 0), blk(sT, 0, 0), AS); break;                 // P10 (part)
+                case 11: mma16(acc, blk(sAqk, 2, 1), blk(sT, 1, 1), AS); break;                 // P21 (part)
+                case 12: mma16(acc, blk(sAqk, 3, 2), blk(sT, 2, 2), AS); break;                 // P32 (part)
+                case 13: mma16(acc, blk(sAqk, 2, 0), blk(sT, 0, 0), AS); break;                 // P20 (part)
+                case 14: mma16(acc, blk(sAqk, 3, 1), blk(sT, 1, 1), AS); break;                 // P31 (part)
+                default: mma16(acc, blk(sAqk, 3, 0), blk(sT, 0, 0), AS); break;                 // P30 (part)
+            }
             __syncthreads();
-            if (warp < 2) t_block(warp + 2, warp);
-            else if (warp == 2) p_block(pA, 2, 1);
-            else if (warp == 3) p_block(pB, 3, 2);
-            else if (warp == 7) p_block(pA, 1, 0);
-            __syncthreads();
-            if (warp == 0) t_block(3, 0);
-            else if (warp == 4) p_block(pB, 2, 0);
-            else if (warp == 5) p_block(pB, 3, 1);
-            __syncthreads();
-            if (warp == 6) p_block(pB, 3, 0);
-            __syncthreads();
-            switch (warp) {
-                case 2: store(pA, blk(sAqk, 2, 1), AS, 1.f); break;
-                case 3: store(pA, blk(sAqk, 0, 0), AS, 1.f); store(pB, blk(sAqk, 3, 2), AS, 1.f); break;
-                case 4: store(pA, blk(sAqk, 1, 1), AS, 1.f); store(pB, blk(sAqk, 2, 0), AS, 1.f); break;
-                case 5: store(pA, blk(sAqk, 2, 2), AS, 1.f); store(pB, blk(sAqk, 3, 1), AS, 1.f); break;
-                case 6: store(pA, blk(sAqk, 3, 3), AS, 1.f); store(pB, blk(sAqk, 3, 0), AS, 1.f); break;
-                case 7: store(pA, blk(sAqk, 1, 0), AS, 1.f); break;
+            switch (warp) {   // level 2: T10, T32 are in
+                case 4: mma16(acc, blk(sAkk, 2, 1), blk(sT, 1, 0), AS); store(acc, blk(sT, 0, 2), AS, 1.f); break;  // Y20
+                case 5: mma16(acc, blk(sAkk, 3, 1), blk(sT, 1, 0), AS); store(acc, blk(sT, 0, 3), AS, 1.f); break;  // Y30
+                case 10: mma16(acc, blk(sAqk, 1, 1), blk(sT, 1, 0), AS); break;                 // P10
+                case 12: mma16(acc, blk(sAqk, 3, 3), blk(sT, 3, 2), AS); break;                 // P32
+                case 13: mma16(acc, blk(sAqk, 2, 1), blk(sT, 1, 0), AS); break;                 // P20 (part)
+                case 15: mma16(acc, blk(sAqk, 3, 1), blk(sT, 1, 0), AS); break;                 // P30 (part)
                 default: break;
+            }
+            __syncthreads();
+            if (warp < 4) {   // level 3: T[2:4, 0:2] = -T[2:4, 2:4] Y
+                const int a_ = 2 + (warp >> 1), b_ = warp & 1;
+                float tt[2][4];
+                zero(tt);
+                mma16(tt, blk(sT, a_, 2), blk(sT, b_, 2), AS);
+                if (a_ == 3) mma16(tt, blk(sT, 3, 3), blk(sT, b_, 3), AS);
+                store(tt, blk(sT, a_, b_), AS, -1.f);
+            }
+            __syncthreads();
+            switch (warp) {   // level 4: T20, T21, T30, T31 are in
+                case 11: mma16(acc, blk(sAqk, 2, 2), blk(sT, 2, 1), AS); break;                 // P21
+                case 13: mma16(acc, blk(sAqk, 2, 2), blk(sT, 2, 0), AS); break;                 // P20
+                case 14: mma16(acc, blk(sAqk, 3, 2), blk(sT, 2, 1), AS);
+                         mma16(acc, blk(sAqk, 3, 3), blk(sT, 3, 1), AS); break;                 // P31
+                case 15: mma16(acc, blk(sAqk, 3, 2), blk(sT, 2, 0), AS);
+                         mma16(acc, blk(sAqk, 3, 3), blk(sT, 3, 0), AS); break;                 // P30
+                default: break;
+            }
+            __syncthreads();
+            if (warp >= 6) {
+                // warp -> its P block: 6..9 the diagonal ones, then 10 (1,0), 11 (2,1),
+                // 12 (3,2), 13 (2,0), 14 (3,1), 15 (3,0)
+                constexpr unsigned long long PA = 0x3323213210ull, PB = 0x0102103210ull;   // 4 bits a warp
+                const int k4 = 4 * (warp - 6);
+                store(acc, blk(sAqk, (int)((PA >> k4) & 15u), (int)((PB >> k4) & 15u)), AS, 1.f);
             }
             __syncthreads();
             // rows of [T ; P] scaled by beta on the columns -> TMEM operand A2
