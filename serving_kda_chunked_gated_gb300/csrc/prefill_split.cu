@@ -444,15 +444,20 @@ prep_kernel(kda_prefill_args a, Work w,
             for (int b = tid >> 7; b < (tid >> 7) + 1; ++b) {   // channel d, sub-chunk b
                 float al[16], kv[16], qv[16], Lc[16];
                 float F1 = 1.f, L = 0.f;
+                const float c1 = -eA * 1.4426950408889634f, c2 = a.g_min * 1.4426950408889634f;   // log2(e)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int t = 16 * b + i;
                     float alpha = 1.f, q = 0.f, k = 0.f;
                     if (t < nc) {
-                        const float g = GATE ? log_decay_softplus(raw_z(t, d), eA)
-                                             : log_decay(raw_z(t, d), eA, a.g_min);
-                        alpha = __expf(g);
-                        L += g;
+                        if (GATE) {
+                            const float g = log_decay_softplus(raw_z(t, d), eA);
+                            alpha = __expf(g);
+                            L += g;
+                        } else {   // exp(g_min Sigmoid(eA z)) in base 2: the two scalings folded
+                            const float sg = __fdividef(1.f, 1.f + exp2f(c1 * raw_z(t, d)));
+                            alpha = exp2f(c2 * sg);
+                        }
                         q = raw_q(t, d) * s_rq[t];
                         k = raw_k(t, d) * s_rk[t];
                     }
