@@ -21,15 +21,18 @@
 //   plan  -- chunk offsets of the packed sequences (exclusive scan of
 //            ceil(len / 64)) into the workspace;
 //   prep  -- persistent, one CTA per SM, a loop over (chunk, head) records:
-//            gate, Gram sub-blocks, blockwise UT solve and MMA 1 (the same
-//            arithmetic as the single-pass kernel), then writes the record
-//            [-W ; Gamma Q - P Gamma K] (tf32 values), [U ; U_o] (fp32),
-//            (K gamma_C / Gamma)^T (tf32 values) and gamma_C;
-//   scan  -- a cluster of two CTAs per (sequence, head), CTA r owning value
-//            columns [64r, 64r+64): per chunk MMA 2 (A from shared memory by
+//            gate, Gram sub-blocks, blockwise UT solve and MMA 1 (the single-
+//            pass kernel's arithmetic; the solve's block merge by doubling),
+//            then writes the record [-W ; Gamma Q - P Gamma K] (fp16, output
+//            rows scaled by powers of two), [U ; U_o] (fp32), (K gamma_C /
+//            Gamma)^T (fp16), gamma_C and the rows' factors, most of it by TMA
+//            stores that drain while the next record runs;
+//   scan  -- a cluster of four CTAs per (sequence, head), CTA r owning value
+//            columns [32r, 32r+32): per chunk MMA 2 (A from shared memory by
 //            TMA, accumulating onto [U ; U_o] preloaded into TMEM), V' to the
 //            MMA 3 operand, O to o and the fused output gate, MMA 3, and the
-//            FP32 state update in TMEM.  The records of the next chunks are
+//            FP32 state update in TMEM, the MMAs on fp16 operands under per-
+//            column power-of-two scaling.  The records of the next chunks are
 //            fetched while the current one is processed.
 #include <mutex>
 
