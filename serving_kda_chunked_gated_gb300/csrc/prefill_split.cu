@@ -809,13 +809,26 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
                 tc::tmem_st16(T0 + TM_A2 + lane_base + c, v);
             }
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
         }
         __syncthreads();   // the Gram tiles are dead from here on
-        // region RB is free: fetch the next record's q, k, z into it
-        if (tid == 0 && has_next && !timed_out) {
-            ++n_in;
-            tc::fence_proxy_async();
-            load_qkz(nxt);
+        // region RB is free: fetch the next record's q, k, z into it; MMA 1's Gamma K
+        // half (its operands are all in) runs while V^T is built
+        bool gk_issued = false;   // thread 0
+        if (tid == 0 && !timed_out) {
+            if (has_next) {
+                ++n_in;
+                tc::fence_proxy_async();
+                load_qkz(nxt);
+            }
+            tc::fence_after_sync();
+            const uint32_t bk = tc::smem_u32(sGK);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(T0 + TM_D + D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bk, D, ks),
+                                tc::idesc_tf32(128, D), 1u);
+            gk_issued = true;
         }
         wait(bar_v, ph_v);
         ph_v ^= 1u;
@@ -852,19 +865,18 @@ prep_kernel(kda_prefill_args a, Work w,
             load_v(nxt);
         }
 
-        // ---- 5. MMA 1: D[:, 0:128] = [T beta ; P beta] . V, D[:, 128:256] += [T beta ; P beta] . Gamma K
-        if (tid == 0 && !timed_out) {
+        // ---- 5. MMA 1: D[:, 0:128] = [T beta ; P beta] . V (the Gamma K half, D[:, 128:256]
+        //         += [T beta ; P beta] . Gamma K, was issued after step 3); one commit for both
+        if (tid == 0 && (gk_issued || !timed_out)) {
+            if (!timed_out) {
+                tc::fence_after_sync();
+                const uint32_t bv = tc::smem_u32(sBpre);
+#pragma unroll
+                for (int ks = 0; ks < C / 8; ++ks)
+                    tc::mma_tf32_ts(T0 + TM_D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bv, D, ks),
+                                    tc::idesc_tf32(128, D), ks > 0);
+            }
             ++n_mma;
-            tc::fence_after_sync();
-            const uint32_t bv = tc::smem_u32(sBpre), bk = tc::smem_u32(sGK);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(T0 + TM_D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bv, D, ks),
-                                tc::idesc_tf32(128, D), ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(T0 + TM_D + D, T0 + TM_A2 + 8 * ks, tc::sw128_desc_k(bk, D, ks),
-                                tc::idesc_tf32(128, D), 1u);
             tc::mma_commit(mbar);
         }
         wait(mbar, ph_mma);
