@@ -47,7 +47,6 @@ constexpr int C = 64;     // chunk length
 constexpr int D = 128;    // dk = dv
 constexpr int NT = 256;   // threads per CTA
 constexpr int AS = 68;    // padded row stride (floats) of the 64x64 Gram tiles
-constexpr int NPAIR = 10; // sub-block pairs (a >= b) of a chunk
 constexpr int SCAN_R = 4; // scan: CTAs (value-column blocks) per (sequence, head)
 
 // one record per (chunk, head), in four arrays of the workspace: the two MMA
@@ -215,8 +214,8 @@ constexpr int OFF_RAWV = OFF_QK + 2 * C * D * 4;    // two [C][64] bf16 tiles, 1
 constexpr int OFF_GK = OFF_RAWV + 2 * C * 64 * 2;   // (Gamma K)^T, SW128 [128 rows][C]
 constexpr int OFF_SMALL = OFF_GK + D * C * 4;
 constexpr int SM_BETA = 0, SM_RQ = 64, SM_RK = 128, SM_TAU = 192, SM_EXPS = SM_TAU + 4 * D,
-              SM_EXPCE = SM_EXPS + 4 * D, SM_GAM = SM_EXPCE + 4 * D, SM_CTAB = SM_GAM + D,
-              SM_DIAG = SM_CTAB + NPAIR * D,            // [4 sub-chunks][9 batches][4 warps][32]
+              SM_GAM = SM_EXPS + 4 * D,
+              SM_DIAG = SM_GAM + D,                     // [4 sub-chunks][9 batches][4 warps][32]
               SM_EA = SM_DIAG + 4 * 9 * 4 * 32,         // exp(A_h) of heads 0..EA_HEADS-1
               SM_LOC = SM_EA + 128,                     // record walk (ints), see prep_kernel
               SM_FLOATS = SM_LOC + 16;
@@ -291,9 +290,7 @@ prep_kernel(kda_prefill_args a, Work w,
     float* s_rk = fs + SM_RK;
     float* s_tau = fs + SM_TAU;
     float* s_expS = fs + SM_EXPS;
-    float* s_expCE = fs + SM_EXPCE;
     float* s_gam = fs + SM_GAM;
-    float* s_ctab = fs + SM_CTAB;
     float* s_diag = fs + SM_DIAG;
     float* s_eA = fs + SM_EA;
     // s_loc: [0..2] this record's {t0, nc, h}, [3..5] the next one's, [6], [7] their
@@ -506,35 +503,9 @@ prep_kernel(kda_prefill_args a, Work w,
                 }
             }
         }
-        __syncthreads();   // raw q/k/z are dead from here on
-        if (tid < D) {
-            const int d = tid;
-            float tau[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) tau[b] = s_tau[b * D + d];
-            float pre = 1.f;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) { s_expS[b * D + d] = pre; pre *= tau[b]; }
-            s_gam[d] = pre;
-            float suf = 1.f;
-#pragma unroll
-            for (int b = 3; b >= 0; --b) { s_expCE[b * D + d] = suf; suf *= tau[b]; }
-#pragma unroll
-            for (int aa = 0; aa < 4; ++aa) {
-#pragma unroll
-                for (int bb = 0; bb <= aa; ++bb) {
-                    float cf = 1.f;
-                    if (aa == bb) cf = __fdividef(1.f, tau[aa]);
-                    else {
-#pragma unroll
-                        for (int m = bb + 1; m < aa; ++m) cf *= tau[m];
-                    }
-                    s_ctab[(aa * (aa + 1) / 2 + bb) * D + d] = cf;
-                }
-            }
-        }
+        // the previous record's A-tile store has read the (Gamma K)^T region, rewritten in step 2
         if (tid == TID_ST && stores_out) { tc::bulk_wait_read(); stores_out = false; }
-        __syncthreads();
+        __syncthreads();   // raw q/k/z are dead from here on
 
         // ---- 2. Gram sub-blocks on the tensor cores.  Block (a, b), b <= a, of A_qk and A_kk is
         //         sum_d q~_i k_j c_ab[d] / k~_i k_j c_ab[d] with k_j = k exp(G_end(b) - G_j) and
@@ -544,24 +515,42 @@ prep_kernel(kda_prefill_args a, Work w,
         //         leaves every block in TMEM, and each row reads the version of its own sub-chunk.
         {
             const int d = tid & (D - 1), b = tid >> 7;
+            // channel d's sub-chunk decays tau_m: es = prod_{m < b}, ec = prod_{m > b},
+            // gamma_C = prod_m, c_ab = prod_{b < m < a} (1 / tau_b for a = b)
+            float tau[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) tau[m] = s_tau[m * D + d];
+            float es = 1.f, ec = 1.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                if (m < b) es *= tau[m];
+#pragma unroll
+            for (int m = 3; m >= 0; --m)
+                if (m > b) ec *= tau[m];
+            s_expS[b * D + d] = es;   // for the -Gamma Q accumulator
+            if (b == 0) s_gam[d] = ((tau[0] * tau[1]) * tau[2]) * tau[3];
 #pragma unroll
             for (int av = 0; av < 4; ++av) {
                 if (av < b) continue;
                 // the softplus gate's diagonal blocks come pair by pair (their factor can overflow)
-                const float cf = (GATE && av == b) ? 0.f : s_ctab[(av * (av + 1) / 2 + b) * D + d];
+                float cf = 1.f;
+                if (av == b) cf = GATE ? 0.f : __fdividef(1.f, tau[b]);
+                else {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        if (m > b && m < av) cf *= tau[m];
+                }
                 const int r0 = kv_row0(av) + 16 * b;
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     *reinterpret_cast<float*>(sKV + tc::sw128_offset(r0 + i, d, KV_ROWS)) = tc::to_tf32(kf2[i] * cf);
             }
             // the record's (K gamma_C / Gamma)^T: row d, the 16 tokens of sub-chunk b
-            const float ec = s_expCE[b * D + d];
             float k16[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) k16[u] = kf2[u] * ec;
             st_stream_h16(w.kt + rec * KT_ELEMS + (size_t)d * C + 16 * b, k16);
             // (Gamma K)^T, MMA 1's second B operand: row d, the 16 tokens of sub-chunk b
-            const float es = s_expS[b * D + d];
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
                 const int t = 16 * b + i;
