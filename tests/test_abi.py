@@ -217,3 +217,23 @@ def test_prefill_from_host_validation(kda_lib):
     assert call(_args(kda, T_total=1000)[0]) == 1                   # no S_T
     assert call(_args(kda, T_total=1000, S_T=FAKE, g_in=FAKE)[0]) == 1   # g_in without y
     assert call(a, st=None) == 8 and call(a, st=FAKE + 8) == 4 and call(a, n=need - 1) == 8
+
+
+def test_record_size_per_chunk_head(kda_lib):
+    """The chunk-parallel workspace holds one record per (chunk, head): the A
+    tile [-W ; Gamma Q - P Gamma K] (128 x 128 fp16), [U ; U_o] (128 x 128
+    fp32), (K gamma_C / Gamma)^T (128 x 64 fp16), gamma_C (128 fp32) and the
+    64 output rows' scale factors (fp32) -- 115456 bytes, the 112.75 KiB per
+    chunk and head that kda.h states; a ragged last chunk takes a whole one."""
+    import serving_kda_chunked_gated_gb300.kda as kda
+    rec = 128 * 128 * 2 + 128 * 128 * 4 + 128 * 64 * 2 + (128 + 64) * 4
+    assert rec == 115456 and rec / 1024 == 112.75
+    sizes, keep = [], []
+    for T in (64 * 10, 64 * 11, 64 * 11 - 5):
+        cu = np.array([0, T], dtype=np.int32)
+        keep.append(cu)
+        a, _ = _args(kda, T_total=T, H=3)
+        a.cu_seqlens_host = cu.ctypes.data
+        sizes.append(kda_lib.kda_prefill_workspace_size(ctypes.byref(a)))
+    assert sizes[1] - sizes[0] == 3 * rec
+    assert sizes[2] == sizes[1]
